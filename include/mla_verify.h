@@ -1,0 +1,192 @@
+/*
+ * mla_verify.h -- C ABI of the GB300 (sm_103a) MLA tree-verify attention library
+ * (libmlaverify.so).
+ *
+ * The operation.  Speculative decoding verifies a tree of T draft tokens per
+ * request in one attention call: every draft token i of request b attends,
+ * for each of H heads, over that request's whole paged latent KV cache under
+ * a tree-visibility mask [Custom sm_120 Verify Kernel, §"The Bottleneck:
+ * Triton's Scattered KV Access at 14 GB/s"; Capture Safety to MoE Ceiling,
+ * §"The Architecture of Capture Safety"].  The cache has page_size = 1, so
+ * each pool row is one token: 512 bf16 latent values followed by 64 bf16
+ * RoPE key values (576 values, 1152 bytes).  With P_b prefix tokens and
+ * L_b = P_b + T keys per request:
+ *
+ *   row(j)   = kv_indices[kv_indptr[b] + j]           for j <  P_b
+ *            = out_cache_loc[b*T + (j - P_b)]         for j >= P_b
+ *   vis(i,j) = bit (mask_indptr[b] + i*L_b + j) of custom_mask, LSB-first
+ *   s_j      = sm_scale * (q_nope[b*T+i, h, :] . kv[row(j), 0:512]
+ *                        + q_rope[b*T+i, h, :] . kv[row(j), 512:576])
+ *   O        = sum_{vis j} softmax(s)_j * kv[row(j), 0:512]
+ *   LSE      = ln sum_{vis j} exp(s_j)
+ *
+ * Prefix rows come from kv_indices and draft rows from out_cache_loc (two
+ * arrays, selected by position), and the mask row stride is P_b + T, not P_b
+ * [Custom sm_120 Verify Kernel, §"The Debugging Gauntlet: Three Real Bugs
+ * Against Live Tensors", bug 2]; mask_indptr holds B entries, one per
+ * request [same section, bug 3].  A token whose visible set is empty gets
+ * O = 0 and LSE = -inf.
+ *
+ * The computation is split-K: each request's key range is cut into `nsplit`
+ * chunks, one CTA per (chunk, group of query rows, request) writes a partial
+ * (normalised O, LSE) into the workspace, and a second kernel merges the
+ * partials by log-sum-exp [Custom sm_120 Verify Kernel, §"Building the
+ * Custom Kernel: From Occupancy Starvation to Flash-Decode"].  The grid is
+ * fixed at plan time and chunk bounds are computed on the device from the
+ * actual lengths; chunks past a request's end exit at once [Capture Safety
+ * to MoE Ceiling, §"The Architecture of Capture Safety"].
+ *
+ * Conventions.
+ *  - All device pointers are borrowed: the caller owns every device buffer,
+ *    the workspace included.  The library owns only the host-side plan.
+ *  - mla_verify_run (and split/merge) allocate nothing, never synchronise
+ *    with the host and only enqueue work on `stream`, so a call can be
+ *    captured into a CUDA graph and replayed with new device contents.
+ *  - Calls return MLA_VERIFY_OK (0) or a positive error code; no exception
+ *    or signal crosses the ABI.  mla_verify_strerror() describes a code.
+ *  - Errors detected on the device (a pool row index outside [0, pool_rows),
+ *    a pipeline wait that timed out) do not abort the call: the offending
+ *    row reads as zeros and a bit is set in a status word inside the
+ *    workspace, read with mla_verify_read_status().
+ *  - One plan may serve concurrent calls on different streams when each
+ *    call has its own workspace.
+ */
+#ifndef MLA_VERIFY_H_
+#define MLA_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define MLA_VERIFY_OK 0
+#define MLA_VERIFY_EINVAL 1       /* bad / NULL / misaligned argument, batch > max_batch */
+#define MLA_VERIFY_EUNSUPPORTED 2 /* d_latent != 512, d_rope != 64, or a device other than sm_103 (the only code the library carries) */
+#define MLA_VERIFY_EWORKSPACE 3   /* workspace missing or smaller than the plan requires */
+#define MLA_VERIFY_ECUDA 4        /* a CUDA runtime call failed (launch, attribute query) */
+
+/* Device status bits (see mla_verify_read_status). */
+#define MLA_VERIFY_DEV_BAD_ROW 0x1u /* some resolved pool row was outside [0, pool_rows) */
+#define MLA_VERIFY_DEV_TIMEOUT 0x2u /* a pipeline wait gave up; that CTA's partial is invalid */
+
+/* Plan flags. */
+#define MLA_VERIFY_FORCE_SIMT 0x1 /* use the CUDA-core (warp-shuffle) split kernel for every shape */
+
+typedef struct mla_verify_plan_s* mla_verify_plan_t; /* opaque, host-only, immutable after plan */
+
+typedef struct {
+  int32_t max_batch;  /* B_max >= 1: largest batch a run may pass; sizes the grid and workspace */
+  int32_t num_heads;  /* H >= 1 */
+  int32_t q_len;      /* T in [1, 64]: draft tokens per request (uniform) */
+  int32_t max_kv_len; /* >= max_b (P_b + T); documents the longest request (chunk size is per request) */
+  int64_t pool_rows;  /* rows in kv_pool; resolved rows outside [0, pool_rows) read as zeros */
+  int32_t nsplit;     /* >= 1: KV chunks per request = partials per output row (fixed grid dimension) */
+  int32_t d_latent;   /* must be 512 */
+  int32_t d_rope;     /* must be 64 */
+  int32_t flags;      /* MLA_VERIFY_FORCE_SIMT or 0 */
+} mla_verify_params;
+
+/* What a plan chose (for tests, benchmarks and logs). */
+typedef struct {
+  int32_t kernel;        /* 1 = tcgen05 tensor-core split kernel, 0 = CUDA-core split kernel */
+  int32_t rows_per_cta;  /* query rows (token x head pairs) one split CTA covers */
+  int32_t keys_per_tile; /* keys per pipeline tile (chunk sizes are multiples of it) */
+  int32_t grid_x, grid_y, grid_z; /* split grid: row groups x nsplit x max_batch */
+  int32_t merge_blocks;  /* merge grid size */
+  int32_t smem_bytes;    /* dynamic shared memory of the split kernel */
+  size_t workspace_bytes;
+} mla_verify_plan_info;
+
+/*
+ * Validate `params` and build a plan.  Host only: touches no device state.
+ * On success *out receives the plan and *workspace_bytes the size of the
+ * device workspace every run with this plan needs (fp32 partial O and LSE
+ * for nsplit x max_batch*q_len*num_heads rows plus a 256-byte header).
+ * The workspace must be 256-byte aligned and zero-filled once before its
+ * first use (e.g. torch.zeros, or mla_verify_workspace_init); the library
+ * keeps the header consistent afterwards.
+ * Errors: EINVAL (NULL pointer, non-positive sizes, q_len > 64),
+ * EUNSUPPORTED (d_latent != 512 or d_rope != 64).
+ */
+int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes,
+                    mla_verify_plan_t* out);
+
+/* Fill *info with the choices of `plan`.  Errors: EINVAL. */
+int mla_verify_plan_describe(mla_verify_plan_t plan, mla_verify_plan_info* info);
+
+/*
+ * One verify call: split kernel then merge kernel, both enqueued on `stream`.
+ *
+ *  q_nope_absorbed  bf16 [batch*q_len, num_heads, 512], contiguous, 16-byte aligned
+ *  q_rope           bf16 [batch*q_len, num_heads, 64],  contiguous, 16-byte aligned
+ *  kv_pool          bf16 [pool_rows, 576], contiguous, 16-byte aligned (rows of 1152 bytes)
+ *  kv_indptr        int32 [batch+1], kv_indptr[0] = 0, non-decreasing; prefix rows only
+ *  kv_indices       int32 [kv_indptr[batch]] pool rows of the prefixes
+ *  out_cache_loc    int32 [batch*q_len] pool rows holding the draft tokens' KV
+ *                   (already written before the call)
+ *  custom_mask      uint8 packed bits, LSB-first; request b's [q_len, P_b+q_len]
+ *                   row-major block starts at bit mask_indptr[b]
+ *  mask_indptr      int32 [batch] bit offsets (B entries, not B+1)
+ *  batch            0 <= batch <= max_batch (0 enqueues nothing)
+ *  sm_scale         score scale (1/sqrt(192) for the K2-class MLA geometry)
+ *  nsplit           must equal the plan's nsplit
+ *  workspace        device buffer of >= the plan's workspace_bytes (see mla_verify_plan)
+ *  o                bf16 [batch*q_len, num_heads, 512] output (round-to-nearest-even)
+ *  lse              fp32 [batch*q_len, num_heads] output, natural log
+ *  stream           cudaStream_t (NULL = legacy default stream)
+ *
+ * The device arrays must stay valid until the enqueued work completes.
+ * Every row the call references, visible or masked, must hold finite values
+ * (a masked key still enters the value product with weight 0).
+ * Errors: EINVAL (NULL or misaligned pointer, batch outside [0, max_batch],
+ * nsplit mismatch), EWORKSPACE, EUNSUPPORTED (device is not sm_103),
+ * ECUDA (launch failure; see mla_verify_strerror).
+ */
+int mla_verify_run(mla_verify_plan_t plan, const void* q_nope_absorbed, const void* q_rope,
+                   const void* kv_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
+                   const int32_t* out_cache_loc, const uint8_t* custom_mask,
+                   const int32_t* mask_indptr, int32_t batch, float sm_scale, int32_t nsplit,
+                   void* workspace, size_t workspace_bytes, void* o, float* lse, void* stream);
+
+/*
+ * The two launches of mla_verify_run, separately: the split kernel (writes
+ * the partials into the workspace) and the merge kernel (reads them, writes
+ * o and lse).  Same arguments and errors as mla_verify_run; merge ignores
+ * the input arrays.  A merge must follow the split of the same call on the
+ * same stream (or be ordered after it).
+ */
+int mla_verify_split(mla_verify_plan_t plan, const void* q_nope_absorbed, const void* q_rope,
+                     const void* kv_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
+                     const int32_t* out_cache_loc, const uint8_t* custom_mask,
+                     const int32_t* mask_indptr, int32_t batch, float sm_scale, int32_t nsplit,
+                     void* workspace, size_t workspace_bytes, void* stream);
+int mla_verify_merge(mla_verify_plan_t plan, int32_t batch, int32_t nsplit, void* workspace,
+                     size_t workspace_bytes, void* o, float* lse, void* stream);
+
+/* Zero the workspace header on `stream` (one cudaMemsetAsync).  Errors: EINVAL, ECUDA. */
+int mla_verify_workspace_init(mla_verify_plan_t plan, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * Synchronise `stream`, then report in *device_status the OR of the
+ * MLA_VERIFY_DEV_* bits raised since the previous read (and clear them).
+ * Test and diagnostics only: it blocks the host, so never call it inside
+ * stream capture.  Errors: EINVAL, ECUDA.
+ */
+int mla_verify_read_status(mla_verify_plan_t plan, void* workspace, void* stream,
+                           uint32_t* device_status);
+
+/* Free the plan (NULL is accepted).  Returns MLA_VERIFY_OK. */
+int mla_verify_destroy(mla_verify_plan_t plan);
+
+/* Static description of a return code, or of the last CUDA error for ECUDA. */
+const char* mla_verify_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_VERIFY_H_ */

@@ -1,0 +1,272 @@
+// C ABI of libmlaverify.so (declared in include/mla_verify.h): argument
+// checks, plan choices, workspace sizing and the two launches per call.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/mla_verify.h"
+#include "common.cuh"
+
+using namespace mlav;
+
+struct mla_verify_plan_s {
+  mla_verify_params p;
+  int kernel;  // 1 = tcgen05, 0 = CUDA cores
+  int nq;      // query rows per split CTA
+  int groups;  // row groups per request
+  int64_t rows_max;
+  size_t off_lse, off_o, ws_bytes;
+  int merge_blocks;
+  int smem;
+};
+
+namespace {
+
+thread_local char g_cuda_msg[256] = "CUDA error";
+
+int cuda_fail(cudaError_t e) {
+  std::snprintf(g_cuda_msg, sizeof g_cuda_msg, "CUDA error %d (%s): %s", (int)e, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return MLA_VERIFY_ECUDA;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Candidate row-group sizes of the tensor-core kernel.  The cost model
+// counts per-key-step tensor time, which is bound by shared-memory operand
+// traffic (a fixed 4 KB key operand plus 32 bytes per query row):
+// ceil(rows/NQ) * (128 + NQ).
+const int kNqChoices[] = {16, 32, 48, 64, 80, 96};
+
+int pick_nq(int rows) {
+  int best = 96;
+  long best_cost = -1;
+  for (int nq : kNqChoices) {
+    const long cost = (long)((rows + nq - 1) / nq) * (128 + nq);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = nq;
+    }
+  }
+  return best;
+}
+
+int tc_smem(int nq) {
+  switch (nq) {
+    case 16: return split_tc_smem_16();
+    case 32: return split_tc_smem_32();
+    case 48: return split_tc_smem_48();
+    case 64: return split_tc_smem_64();
+    case 80: return split_tc_smem_80();
+    default: return split_tc_smem_96();
+  }
+}
+
+cudaError_t tc_launch(int nq, const SplitArgs& a, dim3 grid, cudaStream_t st) {
+  switch (nq) {
+    case 16: return launch_split_tc_16(a, grid, st);
+    case 32: return launch_split_tc_32(a, grid, st);
+    case 48: return launch_split_tc_48(a, grid, st);
+    case 64: return launch_split_tc_64(a, grid, st);
+    case 80: return launch_split_tc_80(a, grid, st);
+    default: return launch_split_tc_96(a, grid, st);
+  }
+}
+
+// Per-device capability check, cached.  The library carries sm_103a code only.
+std::mutex g_dev_mu;
+int g_dev_state[64];  // 0 unknown, 1 ok, 2 unsupported
+
+int check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return MLA_VERIFY_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev_state[dev] == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_dev_state[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return g_dev_state[dev] == 1 ? MLA_VERIFY_OK : MLA_VERIFY_EUNSUPPORTED;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_common(const mla_verify_plan_s* pl, int32_t batch, int32_t nsplit, void* ws, size_t ws_bytes) {
+  if (!pl) return MLA_VERIFY_EINVAL;
+  if (batch < 0 || batch > pl->p.max_batch) return MLA_VERIFY_EINVAL;
+  if (nsplit != pl->p.nsplit) return MLA_VERIFY_EINVAL;
+  if (batch == 0) return MLA_VERIFY_OK;
+  if (!ws || ws_bytes < pl->ws_bytes) return MLA_VERIFY_EWORKSPACE;
+  if (!aligned(ws, 256)) return MLA_VERIFY_EINVAL;
+  return MLA_VERIFY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, mla_verify_plan_t* out) {
+  if (!params || !workspace_bytes || !out) return MLA_VERIFY_EINVAL;
+  const mla_verify_params& p = *params;
+  if (p.max_batch < 1 || p.num_heads < 1 || p.q_len < 1 || p.q_len > kMaxQLen || p.nsplit < 1 ||
+      p.pool_rows < 1 || p.max_kv_len < p.q_len)
+    return MLA_VERIFY_EINVAL;
+  if (p.d_latent != kDLatent || p.d_rope != kDRope) return MLA_VERIFY_EUNSUPPORTED;
+  if ((p.flags & ~MLA_VERIFY_FORCE_SIMT) != 0) return MLA_VERIFY_EINVAL;
+  const int64_t rows_b = (int64_t)p.q_len * p.num_heads;
+  const int64_t rows_max = rows_b * p.max_batch;
+  if (rows_max > (int64_t)1 << 30 || p.pool_rows > ((int64_t)1 << 31) - 1) return MLA_VERIFY_EINVAL;
+
+  mla_verify_plan_s* pl = new (std::nothrow) mla_verify_plan_s();
+  if (!pl) return MLA_VERIFY_EINVAL;
+  pl->p = p;
+  pl->rows_max = rows_max;
+  // Tensor cores unless the request's query rows would leave the smallest
+  // tile (16 columns) at least half padding.
+  pl->kernel = ((p.flags & MLA_VERIFY_FORCE_SIMT) || rows_b <= 8) ? 0 : 1;
+  pl->nq = pl->kernel ? pick_nq((int)rows_b) : kSimtRowsPerCta;
+  pl->groups = (int)((rows_b + pl->nq - 1) / pl->nq);
+  pl->smem = pl->kernel ? tc_smem(pl->nq) : 0;
+  pl->off_lse = kWsHeader;
+  pl->off_o = round_up(pl->off_lse + sizeof(float) * (size_t)p.nsplit * (size_t)rows_max, 256);
+  pl->ws_bytes = pl->off_o + sizeof(float) * (size_t)p.nsplit * (size_t)rows_max * kDLatent;
+  pl->merge_blocks = merge_blocks((int)rows_max);
+  *workspace_bytes = pl->ws_bytes;
+  *out = pl;
+  return MLA_VERIFY_OK;
+}
+
+int mla_verify_plan_describe(mla_verify_plan_t pl, mla_verify_plan_info* info) {
+  if (!pl || !info) return MLA_VERIFY_EINVAL;
+  info->kernel = pl->kernel;
+  info->rows_per_cta = pl->nq;
+  info->keys_per_tile = kKeysPerTile;
+  info->grid_x = pl->groups;
+  info->grid_y = pl->p.nsplit;
+  info->grid_z = pl->p.max_batch;
+  info->merge_blocks = pl->merge_blocks;
+  info->smem_bytes = pl->smem;
+  info->workspace_bytes = pl->ws_bytes;
+  return MLA_VERIFY_OK;
+}
+
+int mla_verify_split(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_rope, const void* kv_pool,
+                     const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* out_cache_loc,
+                     const uint8_t* custom_mask, const int32_t* mask_indptr, int32_t batch, float sm_scale,
+                     int32_t nsplit, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_common(pl, batch, nsplit, workspace, workspace_bytes);
+  if (rc != MLA_VERIFY_OK || batch == 0) return rc;
+  if (!q_nope_absorbed || !q_rope || !kv_pool || !kv_indptr || !out_cache_loc || !custom_mask || !mask_indptr)
+    return MLA_VERIFY_EINVAL;
+  // kv_indices may be NULL only when every prefix is empty; the device never
+  // reads it then.
+  if (!aligned(q_nope_absorbed, 16) || !aligned(q_rope, 16) || !aligned(kv_pool, 16) || !aligned(kv_indptr, 4) ||
+      (kv_indices && !aligned(kv_indices, 4)) || !aligned(out_cache_loc, 4) || !aligned(mask_indptr, 4))
+    return MLA_VERIFY_EINVAL;
+  if (!std::isfinite(sm_scale)) return MLA_VERIFY_EINVAL;
+  if ((rc = check_device()) != MLA_VERIFY_OK) return rc;
+
+  SplitArgs a;
+  a.q_nope = static_cast<const __nv_bfloat16*>(q_nope_absorbed);
+  a.q_rope = static_cast<const __nv_bfloat16*>(q_rope);
+  a.kv_pool = static_cast<const __nv_bfloat16*>(kv_pool);
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.out_cache_loc = out_cache_loc;
+  a.mask = custom_mask;
+  a.mask_indptr = mask_indptr;
+  a.batch = batch;
+  a.H = pl->p.num_heads;
+  a.T = pl->p.q_len;
+  a.nsplit = pl->p.nsplit;
+  a.pool_rows = pl->p.pool_rows;
+  a.rows_max = pl->rows_max;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.part_lse = reinterpret_cast<float*>(ws + pl->off_lse);
+  a.part_o = reinterpret_cast<float*>(ws + pl->off_o);
+
+  const dim3 grid(pl->groups, pl->p.nsplit, pl->p.max_batch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pl->kernel ? tc_launch(pl->nq, a, grid, st) : launch_split_simt(a, grid, st);
+  return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
+}
+
+int mla_verify_merge(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, void* workspace, size_t workspace_bytes,
+                     void* o, float* lse, void* stream) {
+  int rc = check_common(pl, batch, nsplit, workspace, workspace_bytes);
+  if (rc != MLA_VERIFY_OK || batch == 0) return rc;
+  if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return MLA_VERIFY_EINVAL;
+  if ((rc = check_device()) != MLA_VERIFY_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  MergeArgs m;
+  m.rows = batch * pl->p.q_len * pl->p.num_heads;
+  m.nsplit = pl->p.nsplit;
+  m.rows_max = pl->rows_max;
+  m.part_lse = reinterpret_cast<const float*>(ws + pl->off_lse);
+  m.part_o = reinterpret_cast<const float*>(ws + pl->off_o);
+  m.o = static_cast<__nv_bfloat16*>(o);
+  m.lse = lse;
+  m.status = reinterpret_cast<uint32_t*>(ws);
+  cudaError_t e = launch_merge(m, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
+}
+
+int mla_verify_run(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_rope, const void* kv_pool,
+                   const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* out_cache_loc,
+                   const uint8_t* custom_mask, const int32_t* mask_indptr, int32_t batch, float sm_scale,
+                   int32_t nsplit, void* workspace, size_t workspace_bytes, void* o, float* lse, void* stream) {
+  int rc = check_common(pl, batch, nsplit, workspace, workspace_bytes);
+  if (rc != MLA_VERIFY_OK || batch == 0) return rc;
+  if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return MLA_VERIFY_EINVAL;
+  rc = mla_verify_split(pl, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, out_cache_loc, custom_mask,
+                        mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, stream);
+  if (rc != MLA_VERIFY_OK) return rc;
+  return mla_verify_merge(pl, batch, nsplit, workspace, workspace_bytes, o, lse, stream);
+}
+
+int mla_verify_workspace_init(mla_verify_plan_t pl, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!pl || !workspace || workspace_bytes < pl->ws_bytes || !aligned(workspace, 256)) return MLA_VERIFY_EINVAL;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, kWsHeader, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
+}
+
+int mla_verify_read_status(mla_verify_plan_t pl, void* workspace, void* stream, uint32_t* device_status) {
+  if (!pl || !workspace || !device_status) return MLA_VERIFY_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t w[2] = {0, 0};
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(w, workspace, sizeof w, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof w, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *device_status = w[0] | w[1];
+  return MLA_VERIFY_OK;
+}
+
+int mla_verify_destroy(mla_verify_plan_t pl) {
+  delete pl;
+  return MLA_VERIFY_OK;
+}
+
+const char* mla_verify_strerror(int code) {
+  switch (code) {
+    case MLA_VERIFY_OK: return "ok";
+    case MLA_VERIFY_EINVAL: return "invalid argument (NULL, misaligned, out-of-range size or batch, nsplit mismatch)";
+    case MLA_VERIFY_EUNSUPPORTED: return "unsupported: dims must be 512/64 and the device sm_103";
+    case MLA_VERIFY_EWORKSPACE: return "workspace missing or smaller than the plan requires";
+    case MLA_VERIFY_ECUDA: return g_cuda_msg;
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+// Shared definitions of the MLA tree-verify kernels (device and host side).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mlav {
+
+constexpr int kDLatent = 512;
+constexpr int kDRope = 64;
+constexpr int kDRow = kDLatent + kDRope;  // 576 bf16 = 1152 bytes per pool row
+constexpr int kRowBytes = kDRow * 2;
+constexpr int kKeysPerTile = 128;         // keys per pipeline tile; chunk sizes are multiples of it
+constexpr int kMinChunk = 128;
+constexpr int kMaxQLen = 64;
+constexpr int kWsHeader = 256;            // bytes: [0] status accumulated by split, [1] status of the last merge
+
+// Status bits (mirror MLA_VERIFY_DEV_* in mla_verify.h).
+constexpr uint32_t kStatusBadRow = 0x1u;
+constexpr uint32_t kStatusTimeout = 0x2u;
+
+struct SplitArgs {
+  const __nv_bfloat16* q_nope;   // [B*T, H, 512]
+  const __nv_bfloat16* q_rope;   // [B*T, H, 64]
+  const __nv_bfloat16* kv_pool;  // [pool_rows, 576]
+  const int32_t* kv_indptr;      // [B+1]
+  const int32_t* kv_indices;
+  const int32_t* out_cache_loc;  // [B*T]
+  const uint8_t* mask;           // packed bits LSB-first
+  const int32_t* mask_indptr;    // [B] bit offsets
+  int32_t batch, H, T, nsplit;
+  int64_t pool_rows;
+  int64_t rows_max;              // max_batch*T*H: row stride of one split's partials
+  float scale_log2;              // sm_scale * log2(e): scores are kept in base 2
+  float* part_lse;               // [nsplit, rows_max]   natural log, -inf when nothing visible
+  float* part_o;                 // [nsplit, rows_max, 512] normalised partial output
+  uint32_t* status;              // workspace header word 0
+};
+
+struct MergeArgs {
+  int32_t rows;      // batch*T*H rows to produce
+  int32_t nsplit;
+  int64_t rows_max;
+  const float* part_lse;
+  const float* part_o;
+  __nv_bfloat16* o;  // [rows, 512]
+  float* lse;        // [rows]
+  uint32_t* status;  // header words 0 (accumulated) and 1 (last call)
+};
+
+// Key range of split s for a request with L keys: [s*chunk, min(L,(s+1)*chunk)).
+__host__ __device__ inline int64_t chunk_len(int64_t L, int nsplit) {
+  int64_t per = (L + nsplit - 1) / nsplit;
+  int64_t c = (per + kKeysPerTile - 1) / kKeysPerTile * kKeysPerTile;
+  return c < kMinChunk ? kMinChunk : c;
+}
+
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- mbarrier -------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`.  Gives up after ~kWaitLimitNs of
+// wall time or 2^30 polls, whichever comes first, or as soon as another
+// thread of the CTA has raised *abort.  On giving up it raises *abort and the
+// timeout status bit and returns false; callers then skip the rest of their
+// work so every thread reaches the teardown.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  *abort = 1;
+  atomicOr(status, kStatusTimeout);
+  return false;
+}
+
+// ---- cp.async (16-byte, L2-only), zero-filled when src_bytes == 0 ----------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---- index helpers --------------------------------------------------------
+// Pool row of key position j of request b (prefix from kv_indices, drafts
+// from out_cache_loc); -1 when it lies outside [0, pool_rows).
+__device__ __forceinline__ int64_t resolve_row(const SplitArgs& a, int b, int64_t P, int64_t kv_base,
+                                               int64_t j) {
+  int64_t r = (j < P) ? (int64_t)__ldg(a.kv_indices + kv_base + j)
+                      : (int64_t)__ldg(a.out_cache_loc + (int64_t)b * a.T + (j - P));
+  return (r >= 0 && r < a.pool_rows) ? r : -1;
+}
+
+__device__ __forceinline__ uint32_t mask_bit(const uint8_t* mask, int64_t bit) {
+  return (__ldg(mask + (bit >> 3)) >> (bit & 7)) & 1u;
+}
+
+#endif  // __CUDACC__
+
+// Host launchers (defined in the kernel translation units).
+cudaError_t launch_split_simt(const SplitArgs& a, dim3 grid, cudaStream_t stream);
+#define MLAV_DECLARE_TC(NQ)                                                      \
+  cudaError_t launch_split_tc_##NQ(const SplitArgs& a, dim3 grid, cudaStream_t stream); \
+  int split_tc_smem_##NQ();
+MLAV_DECLARE_TC(16)
+MLAV_DECLARE_TC(32)
+MLAV_DECLARE_TC(48)
+MLAV_DECLARE_TC(64)
+MLAV_DECLARE_TC(80)
+MLAV_DECLARE_TC(96)
+#undef MLAV_DECLARE_TC
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+int merge_blocks(int rows);
+
+constexpr int kSimtRowsPerCta = 8;  // one warp per query row
+
+}  // namespace mlav

@@ -1,0 +1,9 @@
+// Tensor-core split kernel instantiated for 32 query rows per CTA.
+#include "split_tc.cuh"
+
+namespace mlav {
+cudaError_t launch_split_tc_32(const SplitArgs& a, dim3 grid, cudaStream_t stream) {
+  return launch_split_tc_nq<32>(a, grid, stream);
+}
+int split_tc_smem_32() { return tc_smem_bytes<32>(); }
+}  // namespace mlav

@@ -1,0 +1,9 @@
+// Tensor-core split kernel instantiated for 96 query rows per CTA.
+#include "split_tc.cuh"
+
+namespace mlav {
+cudaError_t launch_split_tc_96(const SplitArgs& a, dim3 grid, cudaStream_t stream) {
+  return launch_split_tc_nq<96>(a, grid, stream);
+}
+int split_tc_smem_96() { return tc_smem_bytes<96>(); }
+}  // namespace mlav

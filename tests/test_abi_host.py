@@ -1,0 +1,128 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and its host-side validation and plan choices behave as
+documented in include/mla_verify.h."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_speculative_decode_tree_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_speculative_decode_tree_gb300 import build
+    build.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(mla_verify_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_binding_surface():
+    assert declared_functions() == sorted(B.EXPORTED)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_strerror_codes(lib):
+    for code in range(5):
+        assert isinstance(B.strerror(code), str) and B.strerror(code)
+    assert B.strerror(B.MLA_VERIFY_OK) == "ok"
+    assert "unknown" in B.strerror(99)
+
+
+def plan(**kw):
+    args = dict(max_batch=1, num_heads=64, q_len=9, max_kv_len=4105, pool_rows=262144, nsplit=16)
+    args.update(kw)
+    return B.mla_verify_plan(**args)
+
+
+def test_plan_workspace_formula(lib):
+    p = plan(max_batch=2, nsplit=16)
+    rows = 2 * 9 * 64
+    off_o = (256 + 4 * 16 * rows + 255) // 256 * 256
+    assert p.workspace_bytes == off_o + 4 * 16 * rows * 512
+    assert p.describe().workspace_bytes == p.workspace_bytes
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d_latent=256), B.MLA_VERIFY_EUNSUPPORTED),
+    (dict(d_rope=32), B.MLA_VERIFY_EUNSUPPORTED),
+    (dict(q_len=0), B.MLA_VERIFY_EINVAL),
+    (dict(q_len=65), B.MLA_VERIFY_EINVAL),
+    (dict(num_heads=0), B.MLA_VERIFY_EINVAL),
+    (dict(max_batch=0), B.MLA_VERIFY_EINVAL),
+    (dict(nsplit=0), B.MLA_VERIFY_EINVAL),
+    (dict(pool_rows=0), B.MLA_VERIFY_EINVAL),
+    (dict(max_kv_len=3), B.MLA_VERIFY_EINVAL),
+    (dict(flags=0x100), B.MLA_VERIFY_EINVAL),
+])
+def test_plan_rejects(lib, kw, code):
+    with pytest.raises(B.MlaVerifyError) as e:
+        plan(**kw)
+    assert e.value.code == code
+
+
+def test_plan_null_pointers(lib):
+    ws = ctypes.c_size_t(0)
+    h = ctypes.c_void_p(0)
+    assert lib.mla_verify_plan(None, ctypes.byref(ws), ctypes.byref(h)) == B.MLA_VERIFY_EINVAL
+    p = B.MlaVerifyParams(1, 8, 9, 100, 1000, 4, 512, 64, 0)
+    assert lib.mla_verify_plan(ctypes.byref(p), None, ctypes.byref(h)) == B.MLA_VERIFY_EINVAL
+    assert lib.mla_verify_plan_describe(None, None) == B.MLA_VERIFY_EINVAL
+    assert lib.mla_verify_destroy(None) == B.MLA_VERIFY_OK
+
+
+@pytest.mark.parametrize("H,T,flags,kernel,nq", [
+    (64, 9, 0, 1, 96),      # 576 rows -> 6 groups of 96
+    (8, 9, 0, 1, 80),       # 72 rows  -> 1 group of 80
+    (16, 4, 0, 1, 64),      # 64 rows
+    (8, 1, 0, 0, 8),        # decode with 8 heads: tile mostly padding -> CUDA cores
+    (64, 9, B.MLA_VERIFY_FORCE_SIMT, 0, 8),
+])
+def test_plan_kernel_choice(lib, H, T, flags, kernel, nq):
+    info = plan(num_heads=H, q_len=T, max_kv_len=5000 + T, flags=flags).describe()
+    assert info.kernel == kernel
+    assert info.rows_per_cta == nq
+    assert info.grid_x == -(-(H * T) // nq)
+    assert info.grid_y == 16 and info.grid_z == 1
+    if kernel:
+        assert 116 * 1024 < info.smem_bytes <= 227 * 1024  # one CTA per SM
+
+
+FAKE = 0x10000  # never dereferenced: every check below fails before device work
+
+
+def run_raw(lib, p, batch=1, nsplit=None, ws=FAKE, ws_bytes=None, ptr=FAKE, o=FAKE):
+    nsplit = p.nsplit if nsplit is None else nsplit
+    ws_bytes = p.workspace_bytes if ws_bytes is None else ws_bytes
+    return lib.mla_verify_run(ctypes.c_void_p(p.handle), ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, batch, 0.072, nsplit,
+                              ws, ws_bytes, o, o, None)
+
+
+def test_run_host_validation(lib):
+    p = plan(max_batch=2)
+    assert run_raw(lib, p, batch=3) == B.MLA_VERIFY_EINVAL
+    assert run_raw(lib, p, batch=-1) == B.MLA_VERIFY_EINVAL
+    assert run_raw(lib, p, nsplit=8) == B.MLA_VERIFY_EINVAL
+    assert run_raw(lib, p, ws_bytes=p.workspace_bytes - 1) == B.MLA_VERIFY_EWORKSPACE
+    assert run_raw(lib, p, ws=None) == B.MLA_VERIFY_EWORKSPACE
+    assert run_raw(lib, p, ws=FAKE + 16) == B.MLA_VERIFY_EINVAL          # workspace not 256-byte aligned
+    assert run_raw(lib, p, ptr=FAKE + 2) == B.MLA_VERIFY_EINVAL          # q/kv not 16-byte aligned
+    assert run_raw(lib, p, o=FAKE + 8) == B.MLA_VERIFY_EINVAL            # o not 16-byte aligned
+    assert run_raw(lib, p, o=None) == B.MLA_VERIFY_EINVAL
+    assert run_raw(lib, p, batch=0) == B.MLA_VERIFY_OK                   # nothing to enqueue
+    assert lib.mla_verify_merge(ctypes.c_void_p(p.handle), 3, p.nsplit, FAKE, p.workspace_bytes, FAKE, FAKE,
+                                None) == B.MLA_VERIFY_EINVAL
+    assert lib.mla_verify_workspace_init(ctypes.c_void_p(p.handle), FAKE, 16, None) == B.MLA_VERIFY_EINVAL
