@@ -1,0 +1,514 @@
+#!/usr/bin/env python3
+"""Benchmark of the MLA tree-verify call on GB300.
+
+One step = one verify call (split kernel + merge kernel) over one batch of
+synthetic input already resident in HBM.  The headline workload is the
+short-context tree verify (B=1, H=64, 9-token random draft tree, prefix 4096,
+262,144-row pool, NSPLIT=16); the longer-context workloads are reported in
+``sweep``.  L2 is flushed (a 512 MiB device write) before every timed step,
+outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload NAME] [--no-sweep]
+
+For N > 1 it runs under torchrun as N independent replicas (the verify path
+has no exchange step); value = total calls / max-over-ranks time.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = ("verify-attn µs/call, gathered KV GB/s and % roofline at prefix 4k–185k (1 GB300)")
+UNIT = "us/call"
+FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers --
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(cfg) -> str:
+    pre = ("U[%d,%d]" % cfg.prefix) if isinstance(cfg.prefix, tuple) else str(cfg.prefix)
+    return ("%s: B=%d H=%d q_len=%d (%s tree) prefix=%s pool_rows=%d NSPLIT=%d layout=%s"
+            % (cfg.name, cfg.B, cfg.H, cfg.T, cfg.tree, pre, cfg.pool_rows, cfg.nsplit, cfg.layout))
+
+
+def algorithmic(wl):
+    """Algorithmic bytes and FLOPs of one verify call (and of its split kernel)."""
+    T, H = wl["T"], wl["H"]
+    P = np.asarray(wl["prefix_lens"], dtype=np.int64)
+    Lb = P + T
+    N = int(Lb.sum())
+    R = int(len(P) * T * H)
+    mask_bytes = int((T * Lb).sum() // 8)
+    split_bytes = N * 1152 + 4 * int(P.sum()) + 4 * len(P) * T + mask_bytes + R * 1152
+    call_bytes = split_bytes + R * 1028
+    flops = 2 * int((T * H * Lb).sum()) * (576 + 512)
+    return dict(rows=N, kv_bytes=N * 1152, split_bytes=split_bytes, call_bytes=call_bytes, flops=flops)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "mla_speculative_decode_tree_gb300", "csrc")
+    for name in sorted(os.listdir(cdir)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(cdir, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per split-kernel launch from the committed ncu summary, if it matches this source."""
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, log_path=None):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.log_path = log_path
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, what):
+        self.marks.append((what, time.time()))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.log_path:
+            try:
+                with open(self.log_path, "w") as f:
+                    for t, l in self.lines:
+                        f.write("%.3f,%s\n" % (t, l))
+            except OSError:
+                pass
+        t0 = dict(self.marks).get("timed_start")
+        t1 = dict(self.marks).get("timed_end")
+        rows = []
+        for t, l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9 or parts[0] != str(self.gpu):
+                continue
+            rows.append((t, parts))
+        if not rows:
+            return None
+        during = [r for r in rows if t0 is not None and t0 - 0.05 <= r[0] <= (t1 or r[0]) + 0.05]
+        use = during if during else rows
+        sm = [float(p[1]) for _, p in use if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, p in use for k in range(4) if p[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(during)}
+
+
+# ------------------------------------------------------- replica harness ----
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """Max of a per-rank scalar over all ranks (identity on one rank)."""
+    if dist is None or not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_us_per_call(max_total_ms: float, steps: int, world: int) -> float:
+    """Replicas each run `steps` calls; the job processed steps*world calls in max_total_ms."""
+    return max_total_ms * 1e3 / (steps * world)
+
+
+# --------------------------------------------------------------- GPU arm ----
+def time_graph(torch, graph_fn, steps, warmup, flush, stream):
+    """Per-step device time (ms) of graph_fn() with an L2 flush before each step."""
+    times = []
+    with torch.cuda.stream(stream):
+        for it in range(warmup + steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph_fn()
+            e1.record(stream)
+            if it >= warmup:
+                times.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def capture(torch, fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm the allocator / first-call set-up outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False):
+    from mla_speculative_decode_tree_gb300 import binding as B
+    from mla_speculative_decode_tree_gb300 import workloads as W
+
+    cfg = W.CONFIGS[name]
+    wl = W.make_workload(cfg)
+    d = B.device_inputs(wl)
+    v = B.verifier_for(wl)
+    info = v.plan.describe()
+    scale = wl["sm_scale"]
+
+    def call():
+        B.mla_verify_run(v.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
+                         d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], wl["B"], scale, v.plan.nsplit,
+                         v.workspace, v.o, v.lse, stream=stream)
+
+    def split_only():
+        B.mla_verify_split(v.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
+                           d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], wl["B"], scale, v.plan.nsplit,
+                           v.workspace, stream=stream)
+
+    g_call = capture(torch, call, stream)
+    g_split = capture(torch, split_only, stream)
+    t_call = time_graph(torch, g_call.replay, steps, warmup, flush, stream)
+    t_split = time_graph(torch, g_split.replay, steps, warmup, flush, stream)
+    status = v.status(stream)
+    alg = algorithmic(wl)
+    res = dict(wl=wl, info=info, t_call=t_call, t_split=t_split, alg=alg, status=status)
+    if with_e2e:
+        res["e2e"] = measure_e2e(torch, wl, v, stream, steps, warmup, flush)
+    del g_call, g_split, d
+    return res
+
+
+def measure_e2e(torch, wl, v, stream, steps, warmup, flush):
+    """Whole call through the C ABI from pinned host buffers back to pinned host buffers."""
+    from mla_speculative_decode_tree_gb300 import binding as B
+
+    host = {}
+    dev = B.device_inputs(wl)  # the pool stays resident; per-call inputs are re-sent each step
+    per_call = ("q_nope", "q_rope", "kv_indptr", "kv_indices", "out_cache_loc", "custom_mask", "mask_indptr")
+    for k in per_call:
+        host[k] = dev[k].to("cpu").pin_memory()
+    o_h = torch.empty(v.o.shape, dtype=v.o.dtype).pin_memory()
+    l_h = torch.empty(v.lse.shape, dtype=v.lse.dtype).pin_memory()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in per_call)
+    n_out = wl["B"] * wl["T"]
+    d2h = o_h[:n_out].numel() * o_h.element_size() + l_h[:n_out].numel() * l_h.element_size()
+    times = []
+    for it in range(warmup + steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for k in per_call:
+                dev[k].copy_(host[k], non_blocking=True)
+            B.mla_verify_run(v.plan, dev["q_nope"], dev["q_rope"], dev["kv_pool"], dev["kv_indptr"],
+                             dev["kv_indices"], dev["out_cache_loc"], dev["custom_mask"], dev["mask_indptr"],
+                             wl["B"], wl["sm_scale"], v.plan.nsplit, v.workspace, v.o, v.lse, stream=stream)
+            o_h[:n_out].copy_(v.o[:n_out], non_blocking=True)
+            l_h[:n_out].copy_(v.lse[:n_out], non_blocking=True)
+        stream.synchronize()
+        t1 = time.perf_counter()
+        if it >= warmup:
+            times.append((t1 - t0) * 1e3)
+    return dict(times_ms=times, h2d=int(h2d), d2h=int(d2h))
+
+
+def summarize(res, peaks):
+    alg = res["alg"]
+    t_call_us = statistics.mean(res["t_call"]) * 1e3
+    t_split_us = statistics.mean(res["t_split"]) * 1e3
+    hbm = peaks["hbm_gbs"] * 1e9
+    mma = peaks["bf16_tflops"] * 1e12
+    t_hbm = alg["call_bytes"] / hbm * 1e6
+    t_mma = alg["flops"] / mma * 1e6
+    return dict(
+        us_per_call=t_call_us, us_p10=float(np.percentile(res["t_call"], 10) * 1e3),
+        us_p90=float(np.percentile(res["t_call"], 90) * 1e3), split_us=t_split_us,
+        gathered_kv_gbs=alg["kv_bytes"] / (t_call_us * 1e-6) / 1e9,
+        tflops=alg["flops"] / (t_call_us * 1e-6) / 1e12,
+        roofline_frac=max(t_hbm, t_mma) / t_call_us, bound="tensor" if t_mma >= t_hbm else "hbm",
+        kernel="tcgen05" if res["info"].kernel == 1 else "cuda-core", rows_per_cta=res["info"].rows_per_cta,
+        status=res["status"])
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the GPU arm has no CPU fallback)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from __graft_entry__ import build
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+        build()
+
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    phys = torch.cuda.get_device_properties(local)
+    gpu_index = local
+    sampler = ClockSampler(gpu_index, log_path=os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler.start()
+    time.sleep(0.3)
+
+    # ---- headline workload: warm-up + exactly K timed steps, barrier + sync both sides
+    from mla_speculative_decode_tree_gb300 import binding as B
+    from mla_speculative_decode_tree_gb300 import workloads as W
+    cfg = W.CONFIGS[args.workload]
+    wl = W.make_workload(cfg)
+    d = B.device_inputs(wl)
+    v = B.verifier_for(wl)
+    info = v.plan.describe()
+
+    def call():
+        B.mla_verify_run(v.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
+                         d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], wl["B"], wl["sm_scale"],
+                         v.plan.nsplit, v.workspace, v.o, v.lse, stream=stream)
+
+    def split_only():
+        B.mla_verify_split(v.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
+                           d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], wl["B"], wl["sm_scale"],
+                           v.plan.nsplit, v.workspace, stream=stream)
+
+    g_call = capture(torch, call, stream)
+    g_split = capture(torch, split_only, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            g_call.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("timed_start")
+    ev = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g_call.replay()
+            e1.record(stream)
+            ev.append((e0, e1))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("timed_end")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), dist if world > 1 else None, device="cuda")
+    # live split-kernel timing (dominant kernel) on the same stream
+    t_split = time_graph(torch, g_split.replay, args.steps, 3, flush, stream)
+    status = v.status(stream)
+    e2e = measure_e2e(torch, wl, v, stream, args.steps, args.warmup, flush)
+    clocks = sampler.stop()
+
+    alg = algorithmic(wl)
+    us_call = whole_job_us_per_call(total_ms, args.steps, world)
+    split_us = statistics.mean(t_split) * 1e3
+    t_hbm_us = alg["call_bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e6
+    t_mma_us = alg["flops"] / (peaks["bf16_tflops"] * 1e12) * 1e6
+    bound = "tensor" if t_mma_us >= t_hbm_us else "hbm"
+    if bound == "tensor":
+        achieved = alg["flops"] / (split_us * 1e-6) / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved = alg["split_bytes"] / (split_us * 1e-6) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    roofline = {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
+                "kernel": "split (%s, %d query rows/CTA)" % ("tcgen05" if info.kernel else "cuda-core",
+                                                              info.rows_per_cta),
+                "peak_source": "%s (burst: kernel timed alone)" % peak_src,
+                "split_us": round(split_us, 3)}
+    e2e_us = statistics.mean(e2e["times_ms"]) * 1e3 / 1.0
+    line = {
+        "metric": METRIC, "value": round(us_call, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "l2": "flushed (512 MiB write) before every step",
+                   "parallelism": "replicas" if world > 1 else "single GPU", "graph": "split+merge in one CUDA graph"},
+        "gathered_kv_gbs": round(alg["kv_bytes"] / (us_call * world * 1e-6) / 1e9, 2),
+        "roofline_frac_call": round(max(t_hbm_us, t_mma_us) / (us_call * world), 4),
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+        "gpu": phys.name,
+    }
+    if rank == 0 and not args.no_sweep:
+        sweep = {}
+        for name in ("mid64k", "long185k_h8", "batch16_ragged"):
+            try:
+                res = measure_workload(torch, name, min(args.steps, 30), 3, flush, stream)
+                s = summarize(res, peaks)
+                s["traffic"] = ncu_traffic(name)
+                sweep[name] = {k: (round(x, 4) if isinstance(x, float) else x) for k, x in s.items()}
+                del res
+            except Exception as exc:  # keep the headline line even if one sweep entry fails
+                sweep[name] = {"error": repr(exc)[:200]}
+            torch.cuda.empty_cache()
+        line["sweep"] = sweep
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------- oracle (CPU) ----
+def cpu_baseline(wl, budget_s=15.0, rows=None):
+    """Time the fp64 oracle on a bounded sample of output rows; scale to one call."""
+    from oracle import ref
+    ref.build()
+    n_all = wl["B"] * wl["T"] * wl["H"]
+    cores = ref.max_threads()
+    rng = np.random.default_rng(1)
+    if rows is None:
+        probe = np.sort(rng.choice(n_all, size=min(n_all, max(cores, 8)), replace=False))
+        t0 = time.perf_counter()
+        ref.verify(wl, rows=probe, nthreads=cores)
+        per_row = (time.perf_counter() - t0) / probe.size
+        k = int(min(n_all, max(cores, budget_s / max(per_row, 1e-9))))
+        rows = np.sort(rng.choice(n_all, size=k, replace=False))
+    t0 = time.perf_counter()
+    ref.verify(wl, rows=rows, nthreads=cores)
+    dt = time.perf_counter() - t0
+    us_call = dt / rows.size * n_all * 1e6
+    return {"value": round(us_call, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d of %d output rows (token x head) of the workload, fp64, %.1f s wall" % (rows.size, n_all, dt)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return  # rank 0 alone runs the CPU oracle
+    from mla_speculative_decode_tree_gb300 import workloads as W
+    from oracle import ref
+    ref.build()
+    cfg = W.CONFIGS[args.workload]
+    wl = W.make_workload(cfg)
+    n_all = wl["B"] * wl["T"] * wl["H"]
+    cores = ref.max_threads()
+    sample = int(min(n_all, max(cores, 2 * cores)))
+    rng = np.random.default_rng(2)
+    times = []
+    for it in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(n_all, size=sample, replace=False))
+        t0 = time.perf_counter()
+        ref.verify(wl, rows=rows, nthreads=cores)
+        dt = time.perf_counter() - t0
+        if it >= args.warmup:
+            times.append(dt / sample * n_all * 1e6)
+    us = statistics.mean(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "what": "fp64 CPU oracle (no reference code exists to install)"},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d of %d output rows per step, scaled to a whole call" % (sample, n_all)},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--workload", default="short4k")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

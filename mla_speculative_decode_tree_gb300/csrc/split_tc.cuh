@@ -234,13 +234,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
       const int upto = all ? seq : seq - Cfg::kLag;
       for (; retired < upto; ++retired) mbar_arrive(&ctl.full[retired % S]);
     };
-    // Fill one ring slot (blk < 0: the empty filler slot).
+    // Fill one ring slot (blk < 0: the empty filler slot).  Copies are
+    // published (full[] arrivals) kLag slots behind the issue point, and all
+    // of them before this thread blocks on an empty slot: the consumer takes
+    // value blocks two slots at a time, so a block left unpublished while we
+    // wait could be the one it needs to free the slot we wait for.
     auto produce = [&](int blk, int t) {
       if (stop) return;
       const int slot = seq % S;
-      if (!mbar_wait(&ctl.empty[slot], ((seq / S) & 1) ^ 1, &ctl.abort, a.status)) {
-        stop = true;
-        return;
+      const uint32_t par = ((seq / S) & 1) ^ 1;
+      if (!mbar_try_wait(&ctl.empty[slot], par)) {
+        retire(true);
+        if (!mbar_wait(&ctl.empty[slot], par, &ctl.abort, a.status)) {
+          stop = true;
+          return;
+        }
       }
       if (blk >= 0) {
         if (t & 1) issue_block<NQ>(a, sRing + slot * Cfg::kSlotBytes, blk, rowsB, pw, lane);
