@@ -70,7 +70,7 @@ struct TcCfg {
   static constexpr int kOffCtl = kOffRing + kStages * kSlotBytes;
   static constexpr int kOStride = (NQ + 31) / 32 * 32;  // TMEM columns per O^T block (32-aligned)
   static constexpr int kColS = 4 * kOStride;
-  static constexpr int kWords = NQ / 32 + ((NQ % 32) ? 1 : 0);
+  static constexpr int kWords = NQ / 32 + ((NQ % 32) ? 1 : 0);  // 32-column blocks (padded)
 };
 
 template <int NQ>
@@ -347,9 +347,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
     const int j = tid;  // key within the tile == TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16);
     const int64_t mask_base = (int64_t)a.mask_indptr[b] + (int64_t)i0 * L;
-    // Thread n < NQ owns the running sum of query column n (sum of the bf16 P
-    // values it fed to the MMA).
+    // Thread n < NQ owns the running sum of query column n over the bf16 P
+    // values fed to the MMA; it normalises O, so the weights of a split sum to
+    // one exactly.  LSE needs the sum of the unrounded P: lane L of each warp
+    // also keeps, for columns L, L+32, ..., the sum over its warp's keys of the
+    // rounding residuals p - bf16(p).
     float l_col = 0.f;
+    float l_res[Cfg::kWords];
+#pragma unroll
+    for (int w = 0; w < Cfg::kWords; ++w) l_res[w] = 0.f;
     bool my_abort = false;
     for (int t = 0; t < nt; ++t) {
       const int64_t key = j0 + (int64_t)t * kKeysPerTile + j;
@@ -420,6 +426,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
           l_col *= al;
         }
         named_bar_sync(1, kSoftmaxThreads);
+#pragma unroll
+        for (int w = 0; w < Cfg::kWords; ++w)
+          if (32 * w + lane < NQ) l_res[w] *= ctl.alpha[32 * w + lane];
         if (t > 0) {
 #pragma unroll
           for (int n = 0; n < NQ; ++n) rescale |= (ctl.alpha[n] != 1.f);
@@ -461,7 +470,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
           const uint16_t hv = *reinterpret_cast<const uint16_t*>(&hb);
           const uint32_t addr = pbase + n * 128 + ((jc ^ (uint32_t)(n & 7)) << 4);
           asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(hv) : "memory");
+          s[n] = p - __bfloat162float(hb);  // rounding residual of this P
         }
+      }
+      // Sum the residuals over the warp's 32 keys by recursive halving: at
+      // offset o each lane keeps the half of its columns whose bit o matches
+      // its own lane bit and adds the partner's copy, so lane L ends with the
+      // sum for column 32*w + L of each 32-column block w.
+#pragma unroll
+      for (int w = 0; w < Cfg::kWords; ++w) {
+        float v[32];
+#pragma unroll
+        for (int m = 0; m < 32; ++m) v[m] = (32 * w + m < NQ && !my_abort) ? s[32 * w + m] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int m = 0; m < o; ++m) {
+            const float send = upper ? v[m] : v[m + o];
+            const float keep = upper ? v[m + o] : v[m];
+            v[m] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        l_res[w] += v[0];
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -492,6 +523,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
     const bool wa = __any_sync(0xffffffffu, my_abort) || ctl.abort;
     if (lane == 0) ctl.flag[nt & 1][warp] = wa ? 2 : 0;
     if (tid < NQ) ctl.alpha[tid] = l_col;
+#pragma unroll
+    for (int w = 0; w < Cfg::kWords; ++w)
+      if (32 * w + lane < NQ) ctl.red[warp][32 * w + lane] = l_res[w];
     named_bar_sync(1, kSoftmaxThreads);
     const int f = ctl.flag[nt & 1][0] | ctl.flag[nt & 1][1] | ctl.flag[nt & 1][2] | ctl.flag[nt & 1][3];
     if (!(f & 2)) {
@@ -513,7 +547,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
       }
       if (tid < nrows) {
         const float lt = ctl.alpha[tid];
-        lse_out[tid] = lt > 0.f ? (ctl.mref[tid] + __log2f(lt)) * 0.69314718055994530942f : -INFINITY;
+        const float lfull = lt + ((ctl.red[0][tid] + ctl.red[1][tid]) + (ctl.red[2][tid] + ctl.red[3][tid]));
+        lse_out[tid] = lt > 0.f ? (ctl.mref[tid] + __log2f(lfull)) * 0.69314718055994530942f : -INFINITY;
       }
     }
     tc::fence_before_sync();
