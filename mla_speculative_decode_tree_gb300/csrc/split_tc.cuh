@@ -12,7 +12,8 @@
 //   S^T[128 x NQ]       = K_tile[128 x 576] . Q^T        (36 MMAs, K = 16)
 //   O^T[4 x 128 x NQ]  += V^T_tile[512 x 128] . P^T      (4 M-blocks x 8 MMAs)
 // TMEM columns: O^T block m at [m*S_o, m*S_o + NQ) with S_o = NQ rounded up
-// to 32, S^T at [4*S_o, 4*S_o + NQ).
+// to 32, then one or two S^T buffers of NQ columns (two when they fit, so the
+// next tile's scores can be computed while the softmax reads this tile's).
 //
 // Shared memory holds Q (9 blocks of NQ rows x 64 columns, 128-byte
 // swizzled, K-major), P^T (NQ rows x 128 keys, K-major) and a ring of 16 KB
@@ -24,15 +25,20 @@
 // than kept resident: a whole 128-key tile (144 KB) does not fit next to Q.
 //
 // Warp roles (224 threads):
-//   warps 0-3  softmax: TMEM lane quadrant w holds keys 32w..32w+31 of S^T;
-//              mask, running max (raised lazily: only when a score exceeds
-//              it by more than kTau in base 2), exp2, P^T to shared memory,
-//              O^T rescale when the max moves, epilogue.
+//   warps 0-3  softmax: TMEM lane quadrant w holds keys 32w..32w+31 of S^T.
+//              The scores stay in TMEM and are read in 32-column groups by
+//              short loops (a straight-line pass over all columns would not
+//              stay in the instruction cache): pass 1 masks and checks them
+//              against the running max, which is raised only when a score
+//              exceeds it by more than kTau in base 2 (then the exact column
+//              max is reduced and O^T rescaled in TMEM); pass 2 writes
+//              P = exp2(s - m) as bf16 into P^T.  Epilogue: O = O^T / l, LSE.
 //   warp 4     TMEM allocation and the single MMA-issuing thread.
 //   warps 5-6  gather: cp.async 16-byte copies of the rows the split needs,
 //              resolved from kv_indices (prefix) or out_cache_loc (drafts)
 //              [Capture Safety to MoE Ceiling, §"The Architecture of Capture
-//              Safety"], each row's 64-column block placed in swizzled order.
+//              Safety"] into shared memory, each row's 64-column block placed
+//              in swizzled order.
 // Block sequence through the ring: K(0), K(1), V(0), K(2), V(1), ...,
 // K(nt-1), V(nt-2), V(nt-1), where K(t) is the 9 column blocks of tile t and
 // V(t) its first 8 in pairs (one M=128 block of latent columns per pair).  A
@@ -63,28 +69,32 @@ struct TcCfg {
   static constexpr int kPRegion = NQ * 128;  // P^T keys 0..63 or 64..127
   static constexpr int kPBytes = 2 * kPRegion;
   static constexpr int kSlotBytes = 128 * 128;
-  static constexpr int kStages = NQ >= 96 ? 5 : NQ >= 80 ? 7 : NQ >= 64 ? 8 : NQ >= 48 ? 9 : NQ >= 32 ? 10 : 12;
-  static constexpr int kLag = kStages - 1 < 7 ? kStages - 1 : 7;  // cp.async groups left in flight
+  static constexpr int kStages = NQ >= 96 ? 5 : NQ >= 80 ? 6 : NQ >= 64 ? 8 : NQ >= 48 ? 9 : NQ >= 32 ? 10 : 12;
   static constexpr int kOffP = kQBytes;
   static constexpr int kOffRing = kQBytes + kPBytes;
   static constexpr int kOffCtl = kOffRing + kStages * kSlotBytes;
   static constexpr int kOStride = (NQ + 31) / 32 * 32;  // TMEM columns per O^T block (32-aligned)
   static constexpr int kColS = 4 * kOStride;
-  static constexpr int kWords = NQ / 32 + ((NQ % 32) ? 1 : 0);  // 32-column blocks (padded)
+  static constexpr int kSBuf = (kColS + 2 * NQ <= 512) ? 2 : 1;  // S^T buffers
+  static constexpr int kGroups = (NQ + 31) / 32;                 // 32-column groups
 };
 
 template <int NQ>
 struct TcCtl {
   uint64_t full[TcCfg<NQ>::kStages];
   uint64_t empty[TcCfg<NQ>::kStages];
-  uint64_t q_full, s_full, s_free, p_full, pv_done, mma_idle;
+  uint64_t s_full[2], s_free[2];
+  uint64_t q_full, p_full, pv_done, mma_idle;
   uint32_t tmem_base;
   int abort;
   int flag[2][4];
-  alignas(16) float mref[NQ];   // running max per query column (base 2)
-  alignas(16) float alpha[NQ];  // rescale factor of the current tile; column sums in the epilogue
+  int rflag[2];
+  alignas(16) float mtau[NQ];   // running max + kTau (base 2); -inf before any visible key
+  alignas(16) float muse[NQ];   // running max, 0 while it is -inf (all P of the column are 0 then)
+  alignas(16) float alpha[NQ];  // rescale factor of the current tile; 1/l in the epilogue
   alignas(16) float red[4][NQ];
-  uint32_t colmask[kMaxQLen][TcCfg<NQ>::kWords];  // columns owned by each token of the group
+  int rowid[2][kKeysPerTile];   // pool rows of the current / previous tile (-1: zero fill)
+  uint32_t colmask[kMaxQLen][TcCfg<NQ>::kGroups];  // columns owned by each token of the group
 };
 
 template <int NQ>
@@ -101,25 +111,44 @@ __device__ __forceinline__ void mbar_wait_teardown(uint64_t* bar, uint32_t parit
   }
 }
 
-template <int NQ>
-__device__ __forceinline__ void issue_block(const SplitArgs& a, uint32_t slot_addr, int blk, const int (&rows)[16],
-                                            int pw, int lane) {
-  const int c = lane & 7;
-  const int jl = 4 * pw + (lane >> 3);  // key index mod 8 handled by this lane
-  const uint32_t dst0 = slot_addr + jl * 128 + ((c ^ jl) << 4);
-  const __nv_bfloat16* base = a.kv_pool + blk * 64 + c * 8;
+// Sum (or max) of v[0..31] over the 32 lanes of the warp, column by column,
+// by recursive halving: at offset o each lane keeps the half of its values
+// whose index bit o matches its own lane bit and combines it with the
+// partner's copy.  Lane L returns the result for index L.
+template <bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
 #pragma unroll
-  for (int it = 0; it < 16; ++it) {
-    const int row = rows[it];
-    const __nv_bfloat16* src = row >= 0 ? base + (int64_t)row * kDRow : a.kv_pool;
-    cp_async16(dst0 + it * 1024, src, row >= 0 ? 16u : 0u);
+  for (int o = 16; o > 0; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int m = 0; m < o; ++m) {
+      const float send = upper ? v[m] : v[m + o];
+      const float keep = upper ? v[m + o] : v[m];
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[m] = kMax ? fmaxf(keep, got) : keep + got;
+    }
   }
+  return v[0];
+}
+
+// Scores of one 32-column group from TMEM (columns past NQ are not read).
+template <int NQ>
+__device__ __forceinline__ void load_group(uint32_t taddr, int g, float (&v)[32]) {
+  tc::tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(&v[0]));
+  if (32 * g + 16 < NQ) {
+    tc::tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
+  } else {
+#pragma unroll
+    for (int k = 16; k < 32; ++k) v[k] = 0.f;
+  }
+  tc::tmem_wait_ld();
 }
 
 template <int NQ>
 __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
   using Cfg = TcCfg<NQ>;
   constexpr int S = Cfg::kStages;
+  constexpr int SB = Cfg::kSBuf;
   const int b = blockIdx.z;
   if (b >= a.batch) return;
   const int tid = threadIdx.x;
@@ -162,13 +191,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
       mbar_init(&ctl.full[k], kProducerThreads);
       mbar_init(&ctl.empty[k], 1);
     }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&ctl.s_full[k], 1);
+      mbar_init(&ctl.s_free[k], 4);
+    }
     mbar_init(&ctl.q_full, kProducerThreads);
-    mbar_init(&ctl.s_full, 1);
-    mbar_init(&ctl.s_free, 4);
     mbar_init(&ctl.p_full, 4);
     mbar_init(&ctl.pv_done, 1);
     mbar_init(&ctl.mma_idle, 1);
     ctl.abort = 0;
+    ctl.rflag[0] = ctl.rflag[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
@@ -176,9 +208,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
     tc::tmem_relinquish();
   }
   if (tid < kSoftmaxThreads) {
-    for (int n = tid; n < NQ; n += kSoftmaxThreads) ctl.mref[n] = -INFINITY;
-    for (int t = tid; t < kMaxQLen * Cfg::kWords; t += kSoftmaxThreads) {
-      const int tok = t / Cfg::kWords, w = t % Cfg::kWords;
+    for (int n = tid; n < NQ; n += kSoftmaxThreads) {
+      ctl.mtau[n] = -INFINITY;
+      ctl.muse[n] = 0.f;
+    }
+    for (int t = tid; t < ntok * Cfg::kGroups; t += kSoftmaxThreads) {
+      const int tok = t / Cfg::kGroups, w = t % Cfg::kGroups;
       uint32_t bits = 0;
       for (int c = 0; c < 32; ++c) {
         const int n = 32 * w + c;
@@ -196,82 +231,84 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
     // =========================== gather ======================================
     const int pw = warp - kProducerWarp0;
     const int ptid = tid - kProducerWarp0 * 32;
-    // Q rows of the group (zero-filled past the last row).
-    for (int idx = ptid; idx < 9 * NQ * 8; idx += kProducerThreads) {
-      const int blk = idx / (NQ * 8), rem = idx % (NQ * 8), n = rem >> 3, c = rem & 7;
+    // Q rows of the group (zero-filled past the last row): 72 chunks of 16
+    // bytes per row, 64 from q_nope and 8 from q_rope.
+#pragma unroll 2
+    for (int idx = ptid; idx < NQ * 72; idx += kProducerThreads) {
+      const int n = idx / 72, c = idx - n * 72;
       const bool ok = n < nrows;
       const __nv_bfloat16* src =
-          !ok ? a.q_nope
-              : (blk < 8 ? a.q_nope + (grow0 + n) * kDLatent + blk * 64 + c * 8 : a.q_rope + (grow0 + n) * kDRope + c * 8);
-      cp_async16(sQ + blk * Cfg::kQBlock + n * 128 + ((c ^ (n & 7)) << 4), src, ok ? 16u : 0u);
+          !ok ? a.q_nope : (c < 64 ? a.q_nope + (grow0 + n) * kDLatent + c * 8 : a.q_rope + (grow0 + n) * kDRope + (c - 64) * 8);
+      cp_async16(sQ + (c >> 3) * Cfg::kQBlock + n * 128 + (((c & 7) ^ (n & 7)) << 4), src, ok ? 16u : 0u);
     }
-    cp_async_commit();
+    cp_async_arrive(&ctl.q_full);
 
-    int rowsA[16], rowsB[16];
-    int seq = 0, retired = 0;
-    bool q_done = false, stop = false;
+    int seq = 0;
+    bool stop = false;
     uint32_t bad = 0;
-    auto resolve = [&](int t, int (&rows)[16]) {
+    const int c8 = lane & 7;
+    const int jl = 4 * pw + (lane >> 3);  // key index mod 8 this lane copies
+    const uint32_t lane_off = jl * 128 + ((c8 ^ jl) << 4);
+    // Row ids of the keys this warp copies (keys with bit 2 == pw), two per lane.
+    auto resolve = [&](int t) {
+      const int it = lane >> 1;
+      const int q0 = 2 * (lane & 1);
 #pragma unroll
-      for (int it = 0; it < 16; ++it) {
-        const int64_t j = j0 + (int64_t)t * kKeysPerTile + 8 * it + 4 * pw + (lane >> 3);
+      for (int q = 0; q < 2; ++q) {
+        const int jj = 8 * it + 4 * pw + q0 + q;
+        const int64_t j = j0 + (int64_t)t * kKeysPerTile + jj;
         int row = -1;
         if (j < j1) {
           const int64_t rr = resolve_row(a, b, P, kv_base, j);
           if (rr < 0) bad = 1;
           row = (int)rr;
         }
-        rows[it] = row;
+        ctl.rowid[t & 1][jj] = row;
       }
+      __syncwarp();
     };
-    auto retire = [&](bool all) {
-      if (all) cp_async_wait_all(); else cp_async_wait<Cfg::kLag>();
-      fence_proxy_async_smem();
-      if (!q_done) {
-        mbar_arrive(&ctl.q_full);
-        q_done = true;
-      }
-      const int upto = all ? seq : seq - Cfg::kLag;
-      for (; retired < upto; ++retired) mbar_arrive(&ctl.full[retired % S]);
-    };
-    // Fill one ring slot (blk < 0: the empty filler slot).  Copies are
-    // published (full[] arrivals) kLag slots behind the issue point, and all
-    // of them before this thread blocks on an empty slot: the consumer takes
-    // value blocks two slots at a time, so a block left unpublished while we
-    // wait could be the one it needs to free the slot we wait for.
+    // Fill one ring slot (blk < 0: the empty filler slot).  Each thread's
+    // copies are published by an asynchronous arrival on full[slot] that
+    // fires when they have landed, so this warp never waits for memory, only
+    // for a free slot.
     auto produce = [&](int blk, int t) {
       if (stop) return;
       const int slot = seq % S;
-      const uint32_t par = ((seq / S) & 1) ^ 1;
-      if (!mbar_try_wait(&ctl.empty[slot], par)) {
-        retire(true);
-        if (!mbar_wait(&ctl.empty[slot], par, &ctl.abort, a.status)) {
-          stop = true;
-          return;
-        }
+      if (!mbar_wait(&ctl.empty[slot], ((seq / S) & 1) ^ 1, &ctl.abort, a.status)) {
+        stop = true;
+        return;
       }
       if (blk >= 0) {
-        if (t & 1) issue_block<NQ>(a, sRing + slot * Cfg::kSlotBytes, blk, rowsB, pw, lane);
-        else issue_block<NQ>(a, sRing + slot * Cfg::kSlotBytes, blk, rowsA, pw, lane);
+        const uint32_t dst0 = sRing + slot * Cfg::kSlotBytes + lane_off;
+        const __nv_bfloat16* base = a.kv_pool + blk * 64 + c8 * 8;
+        const int* rid = &ctl.rowid[t & 1][jl];
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {
+          const int row = rid[8 * it];
+          cp_async16(dst0 + it * 1024, row >= 0 ? base + (int64_t)row * kDRow : a.kv_pool, row >= 0 ? 16u : 0u);
+        }
+        cp_async_arrive(&ctl.full[slot]);
+      } else {
+        mbar_arrive(&ctl.full[slot]);
       }
-      cp_async_commit();
       ++seq;
-      if (seq >= Cfg::kLag) retire(false);
     };
-    auto produce_v = [&](int t) {
-      for (int pr = 0; pr < 4; ++pr) {
-        if (seq % S == S - 1) produce(-1, t);
-        produce(2 * pr, t);
-        produce(2 * pr + 1, t);
+    for (int t = 0; t <= nt && !stop; ++t) {
+      if (t < nt) {
+        resolve(t);
+#pragma unroll 1
+        for (int blk = 0; blk < 9; ++blk) produce(blk, t);
       }
-    };
-    for (int t = 0; t < nt && !stop; ++t) {
-      if (t & 1) resolve(t, rowsB); else resolve(t, rowsA);
-      for (int blk = 0; blk < 9; ++blk) produce(blk, t);
-      if (t >= 1) produce_v(t - 1);
+      if (t >= 1) {
+#pragma unroll 1
+        for (int pr = 0; pr < 4; ++pr) {
+          if (seq % S == S - 1) produce(-1, t - 1);
+          produce(2 * pr, t - 1);
+          produce(2 * pr + 1, t - 1);
+        }
+      }
     }
-    produce_v(nt - 1);
-    retire(true);
+    cp_async_wait_all();  // nothing in flight when the CTA exits
     if (bad) atomicOr(a.status, kStatusBadRow);
   } else if (warp == kMmaWarp) {
     // ============================ MMA issue ==================================
@@ -279,64 +316,74 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, NQ, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, NQ, true, false);
       int seq = 0;
+      // cp.async writes shared memory through the generic proxy and the MMA
+      // reads it through the async proxy: a proxy fence follows each acquire.
       bool ok = mbar_wait(&ctl.q_full, 0, &ctl.abort, a.status);
+      fence_proxy_async_smem();
       auto take = [&](int& slot) -> bool {
         slot = seq % S;
         const bool r = mbar_wait(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
+        fence_proxy_async_smem();
         tc::fence_after_sync();
         return r;
       };
-      auto do_pv = [&](int u) {
-        if (!ok) return;
-        ok = mbar_wait(&ctl.p_full, u & 1, &ctl.abort, a.status);
-        tc::fence_after_sync();
-        for (int m = 0; m < 4 && ok; ++m) {
-          int sa, sb;
-          if (seq % S == S - 1) {
-            if (!(ok = take(sa))) break;
-            mbar_arrive(&ctl.empty[sa]);
+      for (int t = 0; t <= nt && ok; ++t) {
+        if (t < nt) {
+          // S^T(t) into buffer t % SB once the softmax released it (tile t - SB).
+          const int sb = t % SB;
+          if (t >= SB) {
+            ok = mbar_wait(&ctl.s_free[sb], ((t / SB) & 1) ^ 1, &ctl.abort, a.status);
+            tc::fence_after_sync();
+            if (!ok) break;
+          }
+          const uint32_t d_s = tmem + Cfg::kColS + sb * NQ;
+#pragma unroll 1
+          for (int blk = 0; blk < 9 && ok; ++blk) {
+            int slot;
+            if (!(ok = take(slot))) break;
             ++seq;
-          }
-          if (!(ok = take(sa))) break;
-          ++seq;
-          if (!(ok = take(sb))) break;
-          ++seq;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t adesc =
-                tc::smem_desc(sRing + sa * Cfg::kSlotBytes + kk * 2048, Cfg::kSlotBytes, 1024, tc::kSwizzle128B);
-            const uint64_t bdesc =
-                tc::smem_desc(sP + (kk >> 2) * Cfg::kPRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
-            tc::mma_bf16_ss(tmem + m * Cfg::kOStride, adesc, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t adesc = tc::smem_desc(sRing + slot * Cfg::kSlotBytes + k * 32, 16, 1024, tc::kSwizzle128B);
+              const uint64_t bdesc = tc::smem_desc(sQ + blk * Cfg::kQBlock + k * 32, 16, 1024, tc::kSwizzle128B);
+              tc::mma_bf16_ss(d_s, adesc, bdesc, idesc_qk, (blk | k) ? 1u : 0u);
+            }
+            tc::mma_commit(&ctl.empty[slot]);
           }
-          tc::mma_commit(&ctl.empty[sa]);
-          tc::mma_commit(&ctl.empty[sb]);
-        }
-        if (ok) tc::mma_commit(&ctl.pv_done);
-      };
-      for (int t = 0; t < nt && ok; ++t) {
-        if (t >= 1) {
-          ok = mbar_wait(&ctl.s_free, (t - 1) & 1, &ctl.abort, a.status);
-          tc::fence_after_sync();
           if (!ok) break;
+          tc::mma_commit(&ctl.s_full[sb]);
         }
-        for (int blk = 0; blk < 9 && ok; ++blk) {
-          int slot;
-          if (!(ok = take(slot))) break;
-          ++seq;
+        if (t >= 1) {
+          // O^T += V^T(t-1) . P^T(t-1)
+          const int u = t - 1;
+          ok = mbar_wait(&ctl.p_full, u & 1, &ctl.abort, a.status);
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int m = 0; m < 4 && ok; ++m) {
+            int sa, sb2;
+            if (seq % S == S - 1) {
+              if (!(ok = take(sa))) break;
+              mbar_arrive(&ctl.empty[sa]);
+              ++seq;
+            }
+            if (!(ok = take(sa))) break;
+            ++seq;
+            if (!(ok = take(sb2))) break;
+            ++seq;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t adesc = tc::smem_desc(sRing + slot * Cfg::kSlotBytes + k * 32, 16, 1024, tc::kSwizzle128B);
-            const uint64_t bdesc = tc::smem_desc(sQ + blk * Cfg::kQBlock + k * 32, 16, 1024, tc::kSwizzle128B);
-            tc::mma_bf16_ss(tmem + Cfg::kColS, adesc, bdesc, idesc_qk, (blk | k) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t adesc =
+                  tc::smem_desc(sRing + sa * Cfg::kSlotBytes + kk * 2048, Cfg::kSlotBytes, 1024, tc::kSwizzle128B);
+              const uint64_t bdesc =
+                  tc::smem_desc(sP + (kk >> 2) * Cfg::kPRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
+              tc::mma_bf16_ss(tmem + m * Cfg::kOStride, adesc, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::mma_commit(&ctl.empty[sa]);
+            tc::mma_commit(&ctl.empty[sb2]);
           }
-          tc::mma_commit(&ctl.empty[slot]);
+          if (ok) tc::mma_commit(&ctl.pv_done);
         }
-        if (!ok) break;
-        tc::mma_commit(&ctl.s_full);
-        if (t >= 1) do_pv(t - 1);
       }
-      do_pv(nt - 1);
       // Drain: every MMA this thread issued has completed before TMEM is freed.
       tc::mma_commit(&ctl.mma_idle);
       mbar_wait_teardown(&ctl.mma_idle, 0);
@@ -347,162 +394,162 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
     const int j = tid;  // key within the tile == TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16);
     const int64_t mask_base = (int64_t)a.mask_indptr[b] + (int64_t)i0 * L;
+    const float scale = a.scale_log2;
     // Thread n < NQ owns the running sum of query column n over the bf16 P
     // values fed to the MMA; it normalises O, so the weights of a split sum to
     // one exactly.  LSE needs the sum of the unrounded P: lane L of each warp
-    // also keeps, for columns L, L+32, ..., the sum over its warp's keys of the
-    // rounding residuals p - bf16(p).
+    // also keeps, for columns L, L+32, L+64, the sum over its warp's keys of
+    // the rounding residuals p - bf16(p).
     float l_col = 0.f;
-    float l_res[Cfg::kWords];
-#pragma unroll
-    for (int w = 0; w < Cfg::kWords; ++w) l_res[w] = 0.f;
+    float l_res0 = 0.f, l_res1 = 0.f, l_res2 = 0.f;
+    // P^T is the K-major B operand [NQ rows x 128 keys]: key j lives in region
+    // j/64, 16-byte chunk (j%64)/8 (swizzled by row), element j%8.
+    const uint32_t pbase = sP + (j >> 6) * Cfg::kPRegion + (j & 7) * 2;
+    const uint32_t jc = (j >> 3) & 7;
     bool my_abort = false;
+#pragma unroll 1
     for (int t = 0; t < nt; ++t) {
+      const int sb = t % SB;
+      const uint32_t s_addr = t_lane + Cfg::kColS + sb * NQ;
       const int64_t key = j0 + (int64_t)t * kKeysPerTile + j;
-      uint32_t vis[Cfg::kWords];
-#pragma unroll
-      for (int w = 0; w < Cfg::kWords; ++w) vis[w] = 0;
+      uint32_t vis0 = 0, vis1 = 0, vis2 = 0;
       if (key < j1) {
         for (int tl = 0; tl < ntok; ++tl) {
           if (mask_bit(a.mask, mask_base + (int64_t)tl * L + key)) {
-#pragma unroll
-            for (int w = 0; w < Cfg::kWords; ++w) vis[w] |= ctl.colmask[tl][w];
+            vis0 |= ctl.colmask[tl][0];
+            if (Cfg::kGroups > 1) vis1 |= ctl.colmask[tl][Cfg::kGroups > 1 ? 1 : 0];
+            if (Cfg::kGroups > 2) vis2 |= ctl.colmask[tl][Cfg::kGroups > 2 ? 2 : 0];
           }
         }
       }
-      float s[NQ];
-      if (!my_abort) my_abort = !mbar_wait(&ctl.s_full, t & 1, &ctl.abort, a.status);
+      if (!my_abort) my_abort = !mbar_wait(&ctl.s_full[sb], (t / SB) & 1, &ctl.abort, a.status);
       tc::fence_after_sync();
-      if (!my_abort) {
-#pragma unroll
-        for (int c = 0; c < NQ / 16; ++c) {
-          float v[16];
-          tc::tmem_ld16(t_lane + Cfg::kColS + 16 * c, v);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) s[16 * c + k] = v[k];
-        }
-        tc::tmem_wait_ld();
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0 && !my_abort) mbar_arrive(&ctl.s_free);
 
+      // ---- pass 1: does any score pass the running max by more than kTau?
       bool need = false;
+      if (!my_abort) {
+#pragma unroll 1
+        for (int gq = 0; gq < Cfg::kGroups; ++gq) {
+          float v[32];
+          load_group<NQ>(s_addr + 32 * gq, gq, v);
+          const uint32_t vw = gq == 0 ? vis0 : (gq == 1 ? vis1 : vis2);
+          const float* mt = &ctl.mtau[32 * gq];
 #pragma unroll
-      for (int n = 0; n < NQ; ++n) {
-        const bool v = (vis[n >> 5] >> (n & 31)) & 1u;
-        s[n] = v ? s[n] * a.scale_log2 : -INFINITY;
-        need |= s[n] > ctl.mref[n] + kTau;
+          for (int k = 0; k < 32; ++k) {
+            if (32 * gq + k < NQ) need |= ((vw >> k) & 1u) && (v[k] * scale > mt[k]);
+          }
+        }
       }
       const bool warp_need = __any_sync(0xffffffffu, need);
       const bool warp_abort = __any_sync(0xffffffffu, my_abort) || ctl.abort;
       if (lane == 0) ctl.flag[t & 1][warp] = (warp_need ? 1 : 0) | (warp_abort ? 2 : 0);
       named_bar_sync(1, kSoftmaxThreads);
       const int f = ctl.flag[t & 1][0] | ctl.flag[t & 1][1] | ctl.flag[t & 1][2] | ctl.flag[t & 1][3];
+      if (tid == 0) ctl.rflag[(t + 1) & 1] = 0;
       if (f & 2) {
         my_abort = true;
         break;
       }
       bool rescale = false;
       if (f & 1) {
-        // Raise the running max where a score passed it by more than kTau.
+        // Exact column max over the tile's 128 keys; raise the running max
+        // where it passed by more than kTau.
+#pragma unroll 1
+        for (int gq = 0; gq < Cfg::kGroups; ++gq) {
+          float v[32];
+          load_group<NQ>(s_addr + 32 * gq, gq, v);
+          const uint32_t vw = gq == 0 ? vis0 : (gq == 1 ? vis1 : vis2);
 #pragma unroll
-        for (int n = 0; n < NQ; ++n) {
-          float cm = s[n];
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-          if (lane == 0) ctl.red[warp][n] = cm;
+          for (int k = 0; k < 32; ++k) v[k] = ((vw >> k) & 1u) ? v[k] * scale : -INFINITY;
+          const float cm = warp_transpose_reduce<true>(v, lane);
+          if (32 * gq + lane < NQ) ctl.red[warp][32 * gq + lane] = cm;
         }
         named_bar_sync(1, kSoftmaxThreads);
         if (tid < NQ) {
           const float cm = fmaxf(fmaxf(ctl.red[0][tid], ctl.red[1][tid]), fmaxf(ctl.red[2][tid], ctl.red[3][tid]));
-          const float old = ctl.mref[tid];
+          const float old = ctl.mtau[tid];  // -inf or max + kTau
           float al = 1.f;
-          if (cm > old + kTau) {
-            al = (old == -INFINITY) ? 0.f : ex2_approx(old - cm);
-            ctl.mref[tid] = cm;
+          if (cm > old) {
+            al = (old == -INFINITY) ? 0.f : ex2_approx(old - kTau - cm);
+            ctl.mtau[tid] = cm + kTau;
+            ctl.muse[tid] = cm;
+            ctl.rflag[t & 1] = 1;
           }
           ctl.alpha[tid] = al;
           l_col *= al;
         }
         named_bar_sync(1, kSoftmaxThreads);
-#pragma unroll
-        for (int w = 0; w < Cfg::kWords; ++w)
-          if (32 * w + lane < NQ) l_res[w] *= ctl.alpha[32 * w + lane];
-        if (t > 0) {
-#pragma unroll
-          for (int n = 0; n < NQ; ++n) rescale |= (ctl.alpha[n] != 1.f);
-        }
+        if (lane < NQ) l_res0 *= ctl.alpha[lane];
+        if (32 + lane < NQ) l_res1 *= ctl.alpha[32 + lane];
+        if (64 + lane < NQ) l_res2 *= ctl.alpha[64 + lane];
+        rescale = (t > 0) && ctl.rflag[t & 1];
       }
       // PV of the previous tile must be done before P^T and O^T are touched.
-      if (t >= 1) my_abort = !mbar_wait(&ctl.pv_done, (t - 1) & 1, &ctl.abort, a.status);
+      if (t >= 1 && !my_abort) my_abort = !mbar_wait(&ctl.pv_done, (t - 1) & 1, &ctl.abort, a.status);
       tc::fence_after_sync();
+      if (!my_abort && rescale) {
+#pragma unroll 1
+        for (int c = 0; c < NQ / 16; ++c) {
+          bool any = false;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) any |= ctl.alpha[16 * c + k] != 1.f;
+          if (!any) continue;
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+            float v[16];
+            tc::tmem_ld16(t_lane + m * Cfg::kOStride + 16 * c, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] *= ctl.alpha[16 * c + k];
+            tc::tmem_st16(t_lane + m * Cfg::kOStride + 16 * c, v);
+          }
+        }
+        tc::tmem_wait_st();
+      }
+
+      // ---- pass 2: P = exp2(s - m) -> bf16 into P^T; residual sums for LSE.
       if (!my_abort) {
-        if (rescale) {
+#pragma unroll 1
+        for (int gq = 0; gq < Cfg::kGroups; ++gq) {
+          float v[32];
+          load_group<NQ>(s_addr + 32 * gq, gq, v);
+          const uint32_t vw = gq == 0 ? vis0 : (gq == 1 ? vis1 : vis2);
+          const float* mu = &ctl.muse[32 * gq];
+          const uint32_t prow = pbase + 32 * gq * 128;
 #pragma unroll
-          for (int c = 0; c < NQ / 16; ++c) {
-            bool any = false;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) any |= ctl.alpha[16 * c + k] != 1.f;
-            if (!any) continue;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              float v[16];
-              tc::tmem_ld16(t_lane + m * Cfg::kOStride + 16 * c, v);
-              tc::tmem_wait_ld();
-#pragma unroll
-              for (int k = 0; k < 16; ++k) v[k] *= ctl.alpha[16 * c + k];
-              tc::tmem_st16(t_lane + m * Cfg::kOStride + 16 * c, v);
+          for (int k = 0; k < 32; ++k) {
+            float r = 0.f;
+            if (32 * gq + k < NQ) {
+              const float x = ((vw >> k) & 1u) ? fmaf(v[k], scale, -mu[k]) : -INFINITY;
+              const float p = ex2_approx(x);
+              const __nv_bfloat16 hb = __float2bfloat16_rn(p);
+              const uint16_t hv = *reinterpret_cast<const uint16_t*>(&hb);
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(prow + k * 128 + ((jc ^ (uint32_t)(k & 7)) << 4)), "h"(hv)
+                           : "memory");
+              r = p - __bfloat162float(hb);
             }
+            v[k] = r;
           }
-          tc::tmem_wait_st();
-        }
-        // P = exp2(s - m) as bf16 into P^T, the K-major B operand [NQ rows x
-        // 128 keys]: key j lives in region j/64, 16-byte chunk (j%64)/8
-        // (swizzled by row), element j%8.
-        const uint32_t pbase = sP + (j >> 6) * Cfg::kPRegion + (j & 7) * 2;
-        const uint32_t jc = (j >> 3) & 7;
-#pragma unroll
-        for (int n = 0; n < NQ; ++n) {
-          const float mr = ctl.mref[n];
-          const float p = (mr == -INFINITY) ? 0.f : ex2_approx(s[n] - mr);
-          const __nv_bfloat16 hb = __float2bfloat16_rn(p);
-          const uint16_t hv = *reinterpret_cast<const uint16_t*>(&hb);
-          const uint32_t addr = pbase + n * 128 + ((jc ^ (uint32_t)(n & 7)) << 4);
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(hv) : "memory");
-          s[n] = p - __bfloat162float(hb);  // rounding residual of this P
+          const float rs = warp_transpose_reduce<false>(v, lane);
+          if (gq == 0) l_res0 += rs;
+          else if (gq == 1) l_res1 += rs;
+          else l_res2 += rs;
         }
       }
-      // Sum the residuals over the warp's 32 keys by recursive halving: at
-      // offset o each lane keeps the half of its columns whose bit o matches
-      // its own lane bit and adds the partner's copy, so lane L ends with the
-      // sum for column 32*w + L of each 32-column block w.
-#pragma unroll
-      for (int w = 0; w < Cfg::kWords; ++w) {
-        float v[32];
-#pragma unroll
-        for (int m = 0; m < 32; ++m) v[m] = (32 * w + m < NQ && !my_abort) ? s[32 * w + m] : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const bool upper = (lane & o) != 0;
-#pragma unroll
-          for (int m = 0; m < o; ++m) {
-            const float send = upper ? v[m] : v[m + o];
-            const float keep = upper ? v[m + o] : v[m];
-            v[m] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-          }
-        }
-        l_res[w] += v[0];
-      }
-      fence_proxy_async_smem();
+      // The scores of this tile are no longer needed, nor (after the MMA reads
+      // it) P^T; hand the S^T buffer back and P^T to the MMA.
       tc::fence_before_sync();
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0 && !my_abort) mbar_arrive(&ctl.p_full);
-      // Column sums of this tile's P (the MMA reads P^T concurrently).
+      if (lane == 0 && !my_abort) {
+        mbar_arrive(&ctl.s_free[sb]);
+        mbar_arrive(&ctl.p_full);
+      }
+      // Column sums of this tile's bf16 P (the MMA reads P^T concurrently).
       named_bar_sync(1, kSoftmaxThreads);
       if (tid < NQ && !my_abort) {
         float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
+#pragma unroll 4
         for (int k = 0; k < 16; ++k) {
           const int c = (k + tid) & 7;  // staggered: 8 neighbouring rows hit 8 different chunks
           const uint32_t addr = sP + (k >> 3) * Cfg::kPRegion + tid * 128 + c * 16;
@@ -522,33 +569,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
     tc::fence_after_sync();
     const bool wa = __any_sync(0xffffffffu, my_abort) || ctl.abort;
     if (lane == 0) ctl.flag[nt & 1][warp] = wa ? 2 : 0;
-    if (tid < NQ) ctl.alpha[tid] = l_col;
-#pragma unroll
-    for (int w = 0; w < Cfg::kWords; ++w)
-      if (32 * w + lane < NQ) ctl.red[warp][32 * w + lane] = l_res[w];
+    if (lane < NQ) ctl.red[warp][lane] = l_res0;
+    if (32 + lane < NQ) ctl.red[warp][32 + lane] = l_res1;
+    if (64 + lane < NQ) ctl.red[warp][64 + lane] = l_res2;
     named_bar_sync(1, kSoftmaxThreads);
     const int f = ctl.flag[nt & 1][0] | ctl.flag[nt & 1][1] | ctl.flag[nt & 1][2] | ctl.flag[nt & 1][3];
+    if (tid < NQ) {
+      const float lfull = l_col + ((ctl.red[0][tid] + ctl.red[1][tid]) + (ctl.red[2][tid] + ctl.red[3][tid]));
+      ctl.alpha[tid] = l_col > 0.f ? 1.f / l_col : 0.f;
+      if (!(f & 2) && tid < nrows)
+        lse_out[tid] = l_col > 0.f ? (ctl.muse[tid] + __log2f(lfull)) * 0.69314718055994530942f : -INFINITY;
+    }
+    named_bar_sync(1, kSoftmaxThreads);
     if (!(f & 2)) {
       float* po = a.part_o + ((int64_t)s_idx * a.rows_max + grow0) * kDLatent + j;
-#pragma unroll
+#pragma unroll 1
       for (int m = 0; m < 4; ++m) {
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < NQ / 16; ++c) {
           float v[16];
           tc::tmem_ld16(t_lane + m * Cfg::kOStride + 16 * c, v);
           tc::tmem_wait_ld();
+          const float* inv = &ctl.alpha[16 * c];
+          float* dst = po + (int64_t)(16 * c) * kDLatent + 128 * m;
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const int n = 16 * c + k;
-            const float lt = ctl.alpha[n];
-            if (n < nrows && lt > 0.f) po[(int64_t)n * kDLatent + 128 * m] = v[k] / lt;
+            if (16 * c + k < nrows && inv[k] > 0.f) dst[(int64_t)k * kDLatent] = v[k] * inv[k];
           }
         }
-      }
-      if (tid < nrows) {
-        const float lt = ctl.alpha[tid];
-        const float lfull = lt + ((ctl.red[0][tid] + ctl.red[1][tid]) + (ctl.red[2][tid] + ctl.red[3][tid]));
-        lse_out[tid] = lt > 0.f ? (ctl.mref[tid] + __log2f(lfull)) * 0.69314718055994530942f : -INFINITY;
       }
     }
     tc::fence_before_sync();
