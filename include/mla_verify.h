@@ -45,9 +45,9 @@
  *  - Calls return MLA_VERIFY_OK (0) or a positive error code; no exception
  *    or signal crosses the ABI.  mla_verify_strerror() describes a code.
  *  - Errors detected on the device (a pool row index outside [0, pool_rows),
- *    a pipeline wait that timed out) do not abort the call: the offending
- *    row reads as zeros and a bit is set in a status word inside the
- *    workspace, read with mla_verify_read_status().
+ *    a pipeline wait that timed out) do not abort the call: a key whose
+ *    row is out of range is left out (as if masked) and a bit is set in a
+ *    status word inside the workspace, read with mla_verify_read_status().
  *  - One plan may serve concurrent calls on different streams when each
  *    call has its own workspace.
  */
@@ -82,7 +82,7 @@ typedef struct {
   int32_t num_heads;  /* H >= 1 */
   int32_t q_len;      /* T in [1, 64]: draft tokens per request (uniform) */
   int32_t max_kv_len; /* >= max_b (P_b + T); documents the longest request (chunk size is per request) */
-  int64_t pool_rows;  /* rows in kv_pool; resolved rows outside [0, pool_rows) read as zeros */
+  int64_t pool_rows;  /* rows in kv_pool; keys resolving outside [0, pool_rows) are left out and flagged */
   int32_t nsplit;     /* >= 1: KV chunks per request = partials per output row (fixed grid dimension) */
   int32_t d_latent;   /* must be 512 */
   int32_t d_rope;     /* must be 64 */

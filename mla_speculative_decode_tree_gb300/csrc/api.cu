@@ -1,5 +1,6 @@
 // C ABI of libmlaverify.so (declared in include/mla_verify.h): argument
 // checks, plan choices, workspace sizing and the two launches per call.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -66,15 +67,59 @@ int tc_smem(int nq) {
   }
 }
 
-cudaError_t tc_launch(int nq, const SplitArgs& a, dim3 grid, cudaStream_t st) {
+cudaError_t tc_launch(int nq, const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t st) {
   switch (nq) {
-    case 16: return launch_split_tc_16(a, grid, st);
-    case 32: return launch_split_tc_32(a, grid, st);
-    case 48: return launch_split_tc_48(a, grid, st);
-    case 64: return launch_split_tc_64(a, grid, st);
-    case 80: return launch_split_tc_80(a, grid, st);
-    default: return launch_split_tc_96(a, grid, st);
+    case 16: return launch_split_tc_16(a, m, grid, st);
+    case 32: return launch_split_tc_32(a, m, grid, st);
+    case 48: return launch_split_tc_48(a, m, grid, st);
+    case 64: return launch_split_tc_64(a, m, grid, st);
+    case 80: return launch_split_tc_80(a, m, grid, st);
+    default: return launch_split_tc_96(a, m, grid, st);
   }
+}
+
+// ---- TMA descriptors --------------------------------------------------------
+// cuTensorMapEncodeTiled is a driver entry point; it is fetched through the
+// runtime so the library needs no link-time dependency on libcuda.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::mutex g_enc_mu;
+EncodeTiledFn g_encode = nullptr;
+
+int get_encode(EncodeTiledFn* out) {
+  std::lock_guard<std::mutex> lk(g_enc_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (q != cudaDriverEntryPointSuccess || !fn) {
+      std::snprintf(g_cuda_msg, sizeof g_cuda_msg, "cuTensorMapEncodeTiled is not available from the driver");
+      return MLA_VERIFY_ECUDA;
+    }
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *out = g_encode;
+  return MLA_VERIFY_OK;
+}
+
+// 2-D bf16 tensor [rows, inner] with a row pitch of inner*2 bytes; boxes of
+// box_inner x box_rows elements, 128-byte swizzle, out-of-range reads as 0.
+int encode_bf16_2d(EncodeTiledFn enc, CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                   uint32_t box_inner, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_cuda_msg, sizeof g_cuda_msg, "cuTensorMapEncodeTiled failed with CUresult %d", (int)r);
+    return MLA_VERIFY_ECUDA;
+  }
+  return MLA_VERIFY_OK;
 }
 
 // Per-device capability check, cached.  The library carries sm_103a code only.
@@ -197,7 +242,22 @@ int mla_verify_split(mla_verify_plan_t pl, const void* q_nope_absorbed, const vo
 
   const dim3 grid(pl->groups, pl->p.nsplit, pl->p.max_batch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pl->kernel ? tc_launch(pl->nq, a, grid, st) : launch_split_simt(a, grid, st);
+  cudaError_t e;
+  if (pl->kernel) {
+    // Descriptors are plain host structs passed by value with the launch: no
+    // device work, so this stays capture-safe.
+    EncodeTiledFn enc;
+    if ((rc = get_encode(&enc)) != MLA_VERIFY_OK) return rc;
+    TcMaps maps;
+    const uint64_t rows_total = (uint64_t)batch * pl->p.q_len * pl->p.num_heads;
+    if ((rc = encode_bf16_2d(enc, &maps.kv, kv_pool, kDRow, (uint64_t)pl->p.pool_rows, 64, 1)) != MLA_VERIFY_OK ||
+        (rc = encode_bf16_2d(enc, &maps.qn, q_nope_absorbed, kDLatent, rows_total, 64, pl->nq)) != MLA_VERIFY_OK ||
+        (rc = encode_bf16_2d(enc, &maps.qr, q_rope, kDRope, rows_total, 64, pl->nq)) != MLA_VERIFY_OK)
+      return rc;
+    e = tc_launch(pl->nq, a, maps, grid, st);
+  } else {
+    e = launch_split_simt(a, grid, st);
+  }
   return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
 }
 

@@ -1,6 +1,7 @@
 // Shared definitions of the MLA tree-verify kernels (device and host side).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; encoding goes through the runtime's driver entry point)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -36,6 +37,12 @@ struct SplitArgs {
   float* part_lse;               // [nsplit, rows_max]   natural log, -inf when nothing visible
   float* part_o;                 // [nsplit, rows_max, 512] normalised partial output
   uint32_t* status;              // workspace header word 0
+};
+
+// TMA descriptors of one call: the pool for row gathers (box 64 columns x 1
+// row, 128-byte swizzle) and the two query tensors (box 64 columns x NQ rows).
+struct alignas(64) TcMaps {
+  CUtensorMap kv, qn, qr;
 };
 
 struct MergeArgs {
@@ -157,8 +164,8 @@ __device__ __forceinline__ uint32_t mask_bit(const uint8_t* mask, int64_t bit) {
 
 // Host launchers (defined in the kernel translation units).
 cudaError_t launch_split_simt(const SplitArgs& a, dim3 grid, cudaStream_t stream);
-#define MLAV_DECLARE_TC(NQ)                                                      \
-  cudaError_t launch_split_tc_##NQ(const SplitArgs& a, dim3 grid, cudaStream_t stream); \
+#define MLAV_DECLARE_TC(NQ)                                                                         \
+  cudaError_t launch_split_tc_##NQ(const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t stream); \
   int split_tc_smem_##NQ();
 MLAV_DECLARE_TC(16)
 MLAV_DECLARE_TC(32)

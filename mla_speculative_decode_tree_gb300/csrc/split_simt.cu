@@ -80,8 +80,9 @@ __global__ void __launch_bounds__(32 * kSimtRowsPerCta) split_simt_kernel(SplitA
           va[u] = __ldg(kv + lane);
           vb[u] = __ldg(kv + 32 + lane);
           if (lane < 8) vr[u] = __ldg(kv + 64 + lane);
-        } else if (lane == 0) {
-          atomicOr(a.status, kStatusBadRow);
+        } else {  // a row outside the pool excludes the key
+          vis[u] = false;
+          if (lane == 0) atomicOr(a.status, kStatusBadRow);
         }
       }
     }

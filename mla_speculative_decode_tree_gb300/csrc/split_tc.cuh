@@ -12,11 +12,11 @@
 //   S^T[128 x NQ]       = K_tile[128 x 576] . Q^T        (36 MMAs, K = 16)
 //   O^T[4 x 128 x NQ]  += V^T_tile[512 x 128] . P^T      (4 M-blocks x 8 MMAs)
 // TMEM columns: O^T block m at [m*S_o, m*S_o + NQ) with S_o = NQ rounded up
-// to 32, then one or two S^T buffers of NQ columns (two when they fit, so the
-// next tile's scores can be computed while the softmax reads this tile's).
+// to 32, S^T at [4*S_o, 4*S_o + NQ).
 //
 // Shared memory holds Q (9 blocks of NQ rows x 64 columns, 128-byte
-// swizzled, K-major), P^T (NQ rows x 128 keys, K-major) and a ring of 16 KB
+// swizzled, K-major), two P^T buffers (NQ rows x 128 keys, K-major; tile t
+// writes buffer t%2 while the MMA may still read the other) and a ring of 16 KB
 // slots, each 128 keys x 64 columns of the gathered pool rows in the
 // 128-byte-swizzle atom (8 keys x 128 bytes).  That atom is at once the
 // K-major layout of the key operand and the MN-major layout of the value
@@ -24,21 +24,23 @@
 // tile are fetched a second time (after the next tile's key blocks) rather
 // than kept resident: a whole 128-key tile (144 KB) does not fit next to Q.
 //
-// Warp roles (224 threads):
-//   warps 0-3  softmax: TMEM lane quadrant w holds keys 32w..32w+31 of S^T.
-//              The scores stay in TMEM and are read in 32-column groups by
-//              short loops (a straight-line pass over all columns would not
-//              stay in the instruction cache): pass 1 masks and checks them
-//              against the running max, which is raised only when a score
-//              exceeds it by more than kTau in base 2 (then the exact column
-//              max is reduced and O^T rescaled in TMEM); pass 2 writes
-//              P = exp2(s - m) as bf16 into P^T.  Epilogue: O = O^T / l, LSE.
-//   warp 4     TMEM allocation and the single MMA-issuing thread.
-//   warps 5-6  gather: cp.async 16-byte copies of the rows the split needs,
-//              resolved from kv_indices (prefix) or out_cache_loc (drafts)
-//              [Capture Safety to MoE Ceiling, §"The Architecture of Capture
-//              Safety"] into shared memory, each row's 64-column block placed
-//              in swizzled order.
+// Warp roles (CG = 2 column groups; 32*(4*CG+4) = 384 threads):
+//   warps 0..4CG-1  softmax.  Warp w reads TMEM lane quadrant w%4 (keys
+//              32(w%4)..+31 of the tile) and owns query columns
+//              [(w/4)*NQ/CG, (w/4+1)*NQ/CG).  It loads its scores once (the S^T
+//              buffer is handed back to the MMA right away), masks them,
+//              checks them against the running max -- raised only when a
+//              score exceeds it by more than kTau in base 2, after which the
+//              exact column max is reduced and O^T rescaled in TMEM -- and
+//              writes P = exp2(s - m) as bf16 into P^T.  Per thread and
+//              column it accumulates the bf16 P (normalises O) and the fp32
+//              rounding residual p - bf16(p) (completes LSE).  Epilogue: O^T
+//              scaled by 1/l into shared memory, bulk-stored as 2 KB rows.
+//   warp 4CG   TMEM allocation and the single MMA-issuing thread.
+//   warps 4CG+1..4CG+3  gather, taking turns block by block: TMA
+//              tile::gather4 of four 128-byte row segments per lane, rows resolved from kv_indices (prefix) or out_cache_loc
+//              (drafts) [Capture Safety to MoE Ceiling, §"The Architecture of
+//              Capture Safety"]; Q by 2-D TMA.
 // Block sequence through the ring: K(0), K(1), V(0), K(2), V(1), ...,
 // K(nt-1), V(nt-2), V(nt-1), where K(t) is the 9 column blocks of tile t and
 // V(t) its first 8 in pairs (one M=128 block of latent columns per pair).  A
@@ -54,47 +56,50 @@
 
 namespace mlav {
 
-constexpr int kTcThreads = 224;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kMmaWarp = 4;
-constexpr int kProducerWarp0 = 5;
-constexpr int kProducerThreads = 64;
 constexpr float kTau = 8.0f;  // base-2 headroom before the running max is raised
 
 template <int NQ>
 struct TcCfg {
   static_assert(NQ % 16 == 0 && NQ >= 16 && NQ <= 96, "NQ must be a multiple of 16 in [16, 96]");
+  static constexpr int kCG = 2;                 // softmax warps per TMEM lane quadrant
+  static constexpr int kHC = NQ / kCG;          // query columns per softmax thread
+  static constexpr int kSoftmaxWarps = 4 * kCG;
+  static constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+  static constexpr int kMmaWarp = kSoftmaxWarps;
+  static constexpr int kProducerWarp = kSoftmaxWarps + 1;  // first of kProducerWarps gather warps
+  static constexpr int kProducerWarps = 3;
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProducerWarps);
+  static_assert(kHC % 8 == 0, "columns per softmax thread must be a multiple of 8");
   static constexpr int kQBlock = NQ * 128;  // one 64-column block of Q
   static constexpr int kQBytes = 9 * kQBlock;
   static constexpr int kPRegion = NQ * 128;  // P^T keys 0..63 or 64..127
-  static constexpr int kPBytes = 2 * kPRegion;
+  static constexpr int kPBuf = 2 * kPRegion;  // one P^T buffer; two alternate by tile
+  static constexpr int kPBytes = 2 * kPBuf;
   static constexpr int kSlotBytes = 128 * 128;
-  static constexpr int kStages = NQ >= 96 ? 5 : NQ >= 80 ? 6 : NQ >= 64 ? 8 : NQ >= 48 ? 9 : NQ >= 32 ? 10 : 12;
+  static constexpr int kStages = NQ >= 96 ? 4 : NQ >= 80 ? 5 : NQ >= 64 ? 7 : NQ >= 48 ? 8 : NQ >= 32 ? 10 : 12;
   static constexpr int kOffP = kQBytes;
   static constexpr int kOffRing = kQBytes + kPBytes;
   static constexpr int kOffCtl = kOffRing + kStages * kSlotBytes;
   static constexpr int kOStride = (NQ + 31) / 32 * 32;  // TMEM columns per O^T block (32-aligned)
   static constexpr int kColS = 4 * kOStride;
-  static constexpr int kSBuf = (kColS + 2 * NQ <= 512) ? 2 : 1;  // S^T buffers
-  static constexpr int kGroups = (NQ + 31) / 32;                 // 32-column groups
+  static_assert(NQ * 2048 <= kOffCtl, "epilogue staging must fit below the control block");
 };
 
 template <int NQ>
 struct TcCtl {
   uint64_t full[TcCfg<NQ>::kStages];
   uint64_t empty[TcCfg<NQ>::kStages];
-  uint64_t s_full[2], s_free[2];
-  uint64_t q_full, p_full, pv_done, mma_idle;
+  uint64_t q_full, s_full, s_free, p_full, pv_done[2], mma_idle;
   uint32_t tmem_base;
   int abort;
-  int flag[2][4];
+  int flag[2][12];
   int rflag[2];
   alignas(16) float mtau[NQ];   // running max + kTau (base 2); -inf before any visible key
   alignas(16) float muse[NQ];   // running max, 0 while it is -inf (all P of the column are 0 then)
   alignas(16) float alpha[NQ];  // rescale factor of the current tile; 1/l in the epilogue
   alignas(16) float red[4][NQ];
-  int rowid[2][kKeysPerTile];   // pool rows of the current / previous tile (-1: zero fill)
-  uint32_t colmask[kMaxQLen][TcCfg<NQ>::kGroups];  // columns owned by each token of the group
+  alignas(16) float red2[4][NQ];
+  uint64_t colmask[kMaxQLen][3];  // per token: which of a column group's columns belong to it
 };
 
 template <int NQ>
@@ -111,7 +116,7 @@ __device__ __forceinline__ void mbar_wait_teardown(uint64_t* bar, uint32_t parit
   }
 }
 
-// Sum (or max) of v[0..31] over the 32 lanes of the warp, column by column,
+// Sum (or max) of v[0..31] over the 32 lanes of the warp, index by index,
 // by recursive halving: at offset o each lane keeps the half of its values
 // whose index bit o matches its own lane bit and combines it with the
 // partner's copy.  Lane L returns the result for index L.
@@ -131,24 +136,35 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
   return v[0];
 }
 
-// Scores of one 32-column group from TMEM (columns past NQ are not read).
-template <int NQ>
-__device__ __forceinline__ void load_group(uint32_t taddr, int g, float (&v)[32]) {
-  tc::tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(&v[0]));
-  if (32 * g + 16 < NQ) {
-    tc::tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
-  } else {
+// Reduce per-thread column values x[0..HC) over the warp's 32 lanes and store
+// the result for column c at dst[c] (lane c%32 of group c/32 writes it).
+template <int HC, bool kMax>
+__device__ __forceinline__ void warp_columns_to_smem(const float (&x)[HC], float* dst, int lane) {
 #pragma unroll
-    for (int k = 16; k < 32; ++k) v[k] = 0.f;
+  for (int g = 0; g < (HC + 31) / 32; ++g) {
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const int c = 32 * g + k;
+      v[k] = (c < HC) ? x[c < HC ? c : 0] : (kMax ? -INFINITY : 0.f);
+    }
+    const float r = warp_transpose_reduce<kMax>(v, lane);
+    if (32 * g + lane < HC) dst[32 * g + lane] = r;
   }
-  tc::tmem_wait_ld();
 }
 
 template <int NQ>
-__global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
+__global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
+    split_tc_kernel(const __grid_constant__ SplitArgs a, const __grid_constant__ TcMaps maps) {
   using Cfg = TcCfg<NQ>;
   constexpr int S = Cfg::kStages;
-  constexpr int SB = Cfg::kSBuf;
+  constexpr int HC = Cfg::kHC;
+  constexpr int CG = Cfg::kCG;
+  constexpr int kSoftmaxWarps = Cfg::kSoftmaxWarps;
+  constexpr int kSoftmaxThreads = Cfg::kSoftmaxThreads;
+  constexpr int kMmaWarp = Cfg::kMmaWarp;
+  constexpr int kProducerWarp = Cfg::kProducerWarp;
+  constexpr int kTcThreads = Cfg::kThreads;
   const int b = blockIdx.z;
   if (b >= a.batch) return;
   const int tid = threadIdx.x;
@@ -188,16 +204,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
   // ---- set-up ---------------------------------------------------------------
   if (tid == 0) {
     for (int k = 0; k < S; ++k) {
-      mbar_init(&ctl.full[k], kProducerThreads);
+      mbar_init(&ctl.full[k], 1);
       mbar_init(&ctl.empty[k], 1);
     }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&ctl.s_full[k], 1);
-      mbar_init(&ctl.s_free[k], 4);
-    }
-    mbar_init(&ctl.q_full, kProducerThreads);
-    mbar_init(&ctl.p_full, 4);
-    mbar_init(&ctl.pv_done, 1);
+    mbar_init(&ctl.q_full, 1);
+    mbar_init(&ctl.s_full, 1);
+    mbar_init(&ctl.s_free, kSoftmaxWarps);
+    mbar_init(&ctl.p_full, kSoftmaxWarps);
+    mbar_init(&ctl.pv_done[0], 1);
+    mbar_init(&ctl.pv_done[1], 1);
     mbar_init(&ctl.mma_idle, 1);
     ctl.abort = 0;
     ctl.rflag[0] = ctl.rflag[1] = 0;
@@ -212,14 +227,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
       ctl.mtau[n] = -INFINITY;
       ctl.muse[n] = 0.f;
     }
-    for (int t = tid; t < ntok * Cfg::kGroups; t += kSoftmaxThreads) {
-      const int tok = t / Cfg::kGroups, w = t % Cfg::kGroups;
-      uint32_t bits = 0;
-      for (int c = 0; c < 32; ++c) {
-        const int n = 32 * w + c;
-        if (n < nrows && (r0 + n) / a.H == i0 + tok) bits |= 1u << c;
+    for (int t = tid; t < ntok * CG; t += kSoftmaxThreads) {
+      const int tok = t / CG, h = t % CG;
+      uint64_t bits = 0;
+      for (int c = 0; c < HC; ++c) {
+        const int n = h * HC + c;
+        if (n < nrows && (r0 + n) / a.H == i0 + tok) bits |= 1ull << c;
       }
-      ctl.colmask[tok][w] = bits;
+      ctl.colmask[tok][h] = bits;
     }
   }
   tc::fence_before_sync();
@@ -227,88 +242,81 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
   tc::fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
 
-  if (warp >= kProducerWarp0) {
+  if (warp >= kProducerWarp) {
     // =========================== gather ======================================
-    const int pw = warp - kProducerWarp0;
-    const int ptid = tid - kProducerWarp0 * 32;
-    // Q rows of the group (zero-filled past the last row): 72 chunks of 16
-    // bytes per row, 64 from q_nope and 8 from q_rope.
-#pragma unroll 2
-    for (int idx = ptid; idx < NQ * 72; idx += kProducerThreads) {
-      const int n = idx / 72, c = idx - n * 72;
-      const bool ok = n < nrows;
-      const __nv_bfloat16* src =
-          !ok ? a.q_nope : (c < 64 ? a.q_nope + (grow0 + n) * kDLatent + c * 8 : a.q_rope + (grow0 + n) * kDRope + (c - 64) * 8);
-      cp_async16(sQ + (c >> 3) * Cfg::kQBlock + n * 128 + (((c & 7) ^ (n & 7)) << 4), src, ok ? 16u : 0u);
+    // The producer warps walk the same block sequence and take turns: warp pw
+    // issues the blocks with seq % kProducerWarps == pw (one warp alone cannot
+    // issue row gathers fast enough to keep the tensor cores fed).
+    const int pw = warp - kProducerWarp;
+    if (pw == 0 && lane == 0) {
+      tma::arrive_expect_tx(&ctl.q_full, 9 * Cfg::kQBlock);
+#pragma unroll 1
+      for (int blk = 0; blk < 8; ++blk) tma::load_2d(sQ + blk * Cfg::kQBlock, &maps.qn, blk * 64, (int)grow0, &ctl.q_full);
+      tma::load_2d(sQ + 8 * Cfg::kQBlock, &maps.qr, 0, (int)grow0, &ctl.q_full);
     }
-    cp_async_arrive(&ctl.q_full);
-
+    // Keys past the split's end or resolving outside the pool are fetched
+    // from the split's first row (finite by contract); the softmax masks them.
+    int64_t rsub = resolve_row(a, b, P, kv_base, j0);
+    if (rsub < 0) rsub = 0;
+    int rows[4] = {0, 0, 0, 0}, prev[4] = {0, 0, 0, 0};
+    uint32_t bad = 0;
     int seq = 0;
     bool stop = false;
-    uint32_t bad = 0;
-    const int c8 = lane & 7;
-    const int jl = 4 * pw + (lane >> 3);  // key index mod 8 this lane copies
-    const uint32_t lane_off = jl * 128 + ((c8 ^ jl) << 4);
-    // Row ids of the keys this warp copies (keys with bit 2 == pw), two per lane.
-    auto resolve = [&](int t) {
-      const int it = lane >> 1;
-      const int q0 = 2 * (lane & 1);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int jj = 8 * it + 4 * pw + q0 + q;
-        const int64_t j = j0 + (int64_t)t * kKeysPerTile + jj;
-        int row = -1;
-        if (j < j1) {
-          const int64_t rr = resolve_row(a, b, P, kv_base, j);
-          if (rr < 0) bad = 1;
-          row = (int)rr;
-        }
-        ctl.rowid[t & 1][jj] = row;
-      }
-      __syncwarp();
-    };
-    // Fill one ring slot (blk < 0: the empty filler slot).  Each thread's
-    // copies are published by an asynchronous arrival on full[slot] that
-    // fires when they have landed, so this warp never waits for memory, only
-    // for a free slot.
-    auto produce = [&](int blk, int t) {
+    auto produce = [&](int blk, const int (&r)[4]) {
       if (stop) return;
+      if (seq % Cfg::kProducerWarps != pw) {
+        ++seq;
+        return;
+      }
       const int slot = seq % S;
-      if (!mbar_wait(&ctl.empty[slot], ((seq / S) & 1) ^ 1, &ctl.abort, a.status)) {
+      // every lane acquires the slot; the warp stops together if any gave up
+      const bool got = mbar_wait(&ctl.empty[slot], ((seq / S) & 1) ^ 1, &ctl.abort, a.status);
+      if (!__all_sync(0xffffffffu, got)) {
         stop = true;
         return;
       }
       if (blk >= 0) {
-        const uint32_t dst0 = sRing + slot * Cfg::kSlotBytes + lane_off;
-        const __nv_bfloat16* base = a.kv_pool + blk * 64 + c8 * 8;
-        const int* rid = &ctl.rowid[t & 1][jl];
-#pragma unroll 4
-        for (int it = 0; it < 16; ++it) {
-          const int row = rid[8 * it];
-          cp_async16(dst0 + it * 1024, row >= 0 ? base + (int64_t)row * kDRow : a.kv_pool, row >= 0 ? 16u : 0u);
-        }
-        cp_async_arrive(&ctl.full[slot]);
-      } else {
+        if (lane == 0) tma::arrive_expect_tx(&ctl.full[slot], Cfg::kSlotBytes);
+        __syncwarp();
+        tma::gather4(sRing + slot * Cfg::kSlotBytes + lane * 512, &maps.kv, blk * 64, r[0], r[1], r[2], r[3],
+                     &ctl.full[slot]);
+      } else if (lane == 0) {
         mbar_arrive(&ctl.full[slot]);
       }
       ++seq;
     };
+#pragma unroll 1
     for (int t = 0; t <= nt && !stop; ++t) {
       if (t < nt) {
-        resolve(t);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          prev[q] = rows[q];
+          const int64_t j = j0 + (int64_t)t * kKeysPerTile + 4 * lane + q;
+          int64_t rr = rsub;
+          if (j < j1) {
+            rr = resolve_row(a, b, P, kv_base, j);
+            if (rr < 0) {
+              bad = 1;
+              rr = rsub;
+            }
+          }
+          rows[q] = (int)rr;
+        }
 #pragma unroll 1
-        for (int blk = 0; blk < 9; ++blk) produce(blk, t);
+        for (int blk = 0; blk < 9; ++blk) produce(blk, rows);
       }
       if (t >= 1) {
+        // value blocks of tile t-1: its rows are in prev[] (or still in rows[]
+        // after the last tile)
+        const bool last = (t == nt);
 #pragma unroll 1
         for (int pr = 0; pr < 4; ++pr) {
-          if (seq % S == S - 1) produce(-1, t - 1);
-          produce(2 * pr, t - 1);
-          produce(2 * pr + 1, t - 1);
+          if (seq % S == S - 1) produce(-1, rows);
+          produce(2 * pr, last ? rows : prev);
+          produce(2 * pr + 1, last ? rows : prev);
         }
       }
     }
-    cp_async_wait_all();  // nothing in flight when the CTA exits
     if (bad) atomicOr(a.status, kStatusBadRow);
   } else if (warp == kMmaWarp) {
     // ============================ MMA issue ==================================
@@ -316,27 +324,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, NQ, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, NQ, true, false);
       int seq = 0;
-      // cp.async writes shared memory through the generic proxy and the MMA
-      // reads it through the async proxy: a proxy fence follows each acquire.
       bool ok = mbar_wait(&ctl.q_full, 0, &ctl.abort, a.status);
-      fence_proxy_async_smem();
       auto take = [&](int& slot) -> bool {
         slot = seq % S;
         const bool r = mbar_wait(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
-        fence_proxy_async_smem();
         tc::fence_after_sync();
         return r;
       };
+#pragma unroll 1
       for (int t = 0; t <= nt && ok; ++t) {
         if (t < nt) {
-          // S^T(t) into buffer t % SB once the softmax released it (tile t - SB).
-          const int sb = t % SB;
-          if (t >= SB) {
-            ok = mbar_wait(&ctl.s_free[sb], ((t / SB) & 1) ^ 1, &ctl.abort, a.status);
+          // S^T(t) once the softmax has read S^T(t-1) out of TMEM.
+          if (t >= 1) {
+            ok = mbar_wait(&ctl.s_free, (t - 1) & 1, &ctl.abort, a.status);
             tc::fence_after_sync();
             if (!ok) break;
           }
-          const uint32_t d_s = tmem + Cfg::kColS + sb * NQ;
 #pragma unroll 1
           for (int blk = 0; blk < 9 && ok; ++blk) {
             int slot;
@@ -346,12 +349,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
             for (int k = 0; k < 4; ++k) {
               const uint64_t adesc = tc::smem_desc(sRing + slot * Cfg::kSlotBytes + k * 32, 16, 1024, tc::kSwizzle128B);
               const uint64_t bdesc = tc::smem_desc(sQ + blk * Cfg::kQBlock + k * 32, 16, 1024, tc::kSwizzle128B);
-              tc::mma_bf16_ss(d_s, adesc, bdesc, idesc_qk, (blk | k) ? 1u : 0u);
+              tc::mma_bf16_ss(tmem + Cfg::kColS, adesc, bdesc, idesc_qk, (blk | k) ? 1u : 0u);
             }
             tc::mma_commit(&ctl.empty[slot]);
           }
           if (!ok) break;
-          tc::mma_commit(&ctl.s_full[sb]);
+          tc::mma_commit(&ctl.s_full);
         }
         if (t >= 1) {
           // O^T += V^T(t-1) . P^T(t-1)
@@ -360,7 +363,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
           tc::fence_after_sync();
 #pragma unroll 1
           for (int m = 0; m < 4 && ok; ++m) {
-            int sa, sb2;
+            int sa, sb;
             if (seq % S == S - 1) {
               if (!(ok = take(sa))) break;
               mbar_arrive(&ctl.empty[sa]);
@@ -368,20 +371,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
             }
             if (!(ok = take(sa))) break;
             ++seq;
-            if (!(ok = take(sb2))) break;
+            if (!(ok = take(sb))) break;
             ++seq;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t adesc =
                   tc::smem_desc(sRing + sa * Cfg::kSlotBytes + kk * 2048, Cfg::kSlotBytes, 1024, tc::kSwizzle128B);
               const uint64_t bdesc =
-                  tc::smem_desc(sP + (kk >> 2) * Cfg::kPRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
+                  tc::smem_desc(sP + (u & 1) * Cfg::kPBuf + (kk >> 2) * Cfg::kPRegion + (kk & 3) * 32, 16, 1024,
+                                tc::kSwizzle128B);
               tc::mma_bf16_ss(tmem + m * Cfg::kOStride, adesc, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
             }
             tc::mma_commit(&ctl.empty[sa]);
-            tc::mma_commit(&ctl.empty[sb2]);
+            tc::mma_commit(&ctl.empty[sb]);
           }
-          if (ok) tc::mma_commit(&ctl.pv_done);
+          if (ok) tc::mma_commit(&ctl.pv_done[u & 1]);
         }
       }
       // Drain: every MMA this thread issued has completed before TMEM is freed.
@@ -391,60 +395,71 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
     __syncwarp();
   } else {
     // ============================ softmax ====================================
-    const int j = tid;  // key within the tile == TMEM lane
-    const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16);
+    const int quad = warp & 3;
+    const int half = warp >> 2;  // column group
+    const int j = 32 * quad + lane;  // key within the tile == TMEM lane
+    const int c0 = half * HC;        // first query column of this thread
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * quad) << 16);
     const int64_t mask_base = (int64_t)a.mask_indptr[b] + (int64_t)i0 * L;
     const float scale = a.scale_log2;
-    // Thread n < NQ owns the running sum of query column n over the bf16 P
-    // values fed to the MMA; it normalises O, so the weights of a split sum to
-    // one exactly.  LSE needs the sum of the unrounded P: lane L of each warp
-    // also keeps, for columns L, L+32, L+64, the sum over its warp's keys of
-    // the rounding residuals p - bf16(p).
-    float l_col = 0.f;
-    float l_res0 = 0.f, l_res1 = 0.f, l_res2 = 0.f;
+    // Column sums.  Thread tid < 2*NQ sums half-row tid of P^T (column tid/2,
+    // keys 64*(tid%2)..+63) over the tiles: the bf16 P fed to the MMA, which
+    // normalises O so a split's weights sum to one exactly.  Each thread also
+    // keeps, per own column, the fp32 residuals p - bf16(p) of its key, for
+    // LSE from the unrounded sum.
+    float l_half = 0.f;
+    float acc_r[HC];
+#pragma unroll
+    for (int k = 0; k < HC; ++k) acc_r[k] = 0.f;
     // P^T is the K-major B operand [NQ rows x 128 keys]: key j lives in region
     // j/64, 16-byte chunk (j%64)/8 (swizzled by row), element j%8.
-    const uint32_t pbase = sP + (j >> 6) * Cfg::kPRegion + (j & 7) * 2;
+    const uint32_t pbase = sP + (j >> 6) * Cfg::kPRegion + (j & 7) * 2 + c0 * 128;
     const uint32_t jc = (j >> 3) & 7;
     bool my_abort = false;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
-      const int sb = t % SB;
-      const uint32_t s_addr = t_lane + Cfg::kColS + sb * NQ;
       const int64_t key = j0 + (int64_t)t * kKeysPerTile + j;
-      uint32_t vis0 = 0, vis1 = 0, vis2 = 0;
-      if (key < j1) {
-        for (int tl = 0; tl < ntok; ++tl) {
-          if (mask_bit(a.mask, mask_base + (int64_t)tl * L + key)) {
-            vis0 |= ctl.colmask[tl][0];
-            if (Cfg::kGroups > 1) vis1 |= ctl.colmask[tl][Cfg::kGroups > 1 ? 1 : 0];
-            if (Cfg::kGroups > 2) vis2 |= ctl.colmask[tl][Cfg::kGroups > 2 ? 2 : 0];
-          }
-        }
+      uint64_t vis = 0;
+      if (key < j1 && resolve_row(a, b, P, kv_base, key) >= 0) {  // rows outside the pool are excluded
+        for (int tl = 0; tl < ntok; ++tl)
+          if (mask_bit(a.mask, mask_base + (int64_t)tl * L + key)) vis |= ctl.colmask[tl][half];
       }
-      if (!my_abort) my_abort = !mbar_wait(&ctl.s_full[sb], (t / SB) & 1, &ctl.abort, a.status);
+      float s[HC];
+      if (!my_abort) my_abort = !mbar_wait(&ctl.s_full, t & 1, &ctl.abort, a.status);
+      my_abort = __any_sync(0xffffffffu, my_abort);  // tcgen05.ld below is warp-collective
       tc::fence_after_sync();
-
-      // ---- pass 1: does any score pass the running max by more than kTau?
-      bool need = false;
       if (!my_abort) {
-#pragma unroll 1
-        for (int gq = 0; gq < Cfg::kGroups; ++gq) {
-          float v[32];
-          load_group<NQ>(s_addr + 32 * gq, gq, v);
-          const uint32_t vw = gq == 0 ? vis0 : (gq == 1 ? vis1 : vis2);
-          const float* mt = &ctl.mtau[32 * gq];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (32 * gq + k < NQ) need |= ((vw >> k) & 1u) && (v[k] * scale > mt[k]);
-          }
+        for (int c = 0; c < HC / 8; ++c) tc::tmem_ld8(t_lane + Cfg::kColS + c0 + 8 * c, &s[8 * c]);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int k = 0; k < HC; ++k) s[k] = 0.f;
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0 && !my_abort) mbar_arrive(&ctl.s_free);  // S^T may be overwritten now
+
+      bool need = false;
+      const float4* mt4 = reinterpret_cast<const float4*>(&ctl.mtau[c0]);
+#pragma unroll
+      for (int k4 = 0; k4 < HC / 4; ++k4) {
+        const float4 mt = mt4[k4];
+        const float mtk[4] = {mt.x, mt.y, mt.z, mt.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int k = 4 * k4 + q;
+          s[k] = ((vis >> k) & 1ull) ? s[k] * scale : -INFINITY;
+          need |= s[k] > mtk[q];
         }
       }
       const bool warp_need = __any_sync(0xffffffffu, need);
       const bool warp_abort = __any_sync(0xffffffffu, my_abort) || ctl.abort;
       if (lane == 0) ctl.flag[t & 1][warp] = (warp_need ? 1 : 0) | (warp_abort ? 2 : 0);
       named_bar_sync(1, kSoftmaxThreads);
-      const int f = ctl.flag[t & 1][0] | ctl.flag[t & 1][1] | ctl.flag[t & 1][2] | ctl.flag[t & 1][3];
+      int f = 0;
+#pragma unroll
+      for (int w = 0; w < kSoftmaxWarps; ++w) f |= ctl.flag[t & 1][w];
       if (tid == 0) ctl.rflag[(t + 1) & 1] = 0;
       if (f & 2) {
         my_abort = true;
@@ -454,16 +469,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
       if (f & 1) {
         // Exact column max over the tile's 128 keys; raise the running max
         // where it passed by more than kTau.
-#pragma unroll 1
-        for (int gq = 0; gq < Cfg::kGroups; ++gq) {
-          float v[32];
-          load_group<NQ>(s_addr + 32 * gq, gq, v);
-          const uint32_t vw = gq == 0 ? vis0 : (gq == 1 ? vis1 : vis2);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = ((vw >> k) & 1u) ? v[k] * scale : -INFINITY;
-          const float cm = warp_transpose_reduce<true>(v, lane);
-          if (32 * gq + lane < NQ) ctl.red[warp][32 * gq + lane] = cm;
-        }
+        warp_columns_to_smem<HC, true>(s, &ctl.red[quad][c0], lane);
         named_bar_sync(1, kSoftmaxThreads);
         if (tid < NQ) {
           const float cm = fmaxf(fmaxf(ctl.red[0][tid], ctl.red[1][tid]), fmaxf(ctl.red[2][tid], ctl.red[3][tid]));
@@ -476,127 +482,134 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
             ctl.rflag[t & 1] = 1;
           }
           ctl.alpha[tid] = al;
-          l_col *= al;
         }
         named_bar_sync(1, kSoftmaxThreads);
-        if (lane < NQ) l_res0 *= ctl.alpha[lane];
-        if (32 + lane < NQ) l_res1 *= ctl.alpha[32 + lane];
-        if (64 + lane < NQ) l_res2 *= ctl.alpha[64 + lane];
+#pragma unroll
+        for (int k = 0; k < HC; ++k) acc_r[k] *= ctl.alpha[c0 + k];
+        if (tid < 2 * NQ) l_half *= ctl.alpha[tid >> 1];
         rescale = (t > 0) && ctl.rflag[t & 1];
       }
-      // PV of the previous tile must be done before P^T and O^T are touched.
-      if (t >= 1 && !my_abort) my_abort = !mbar_wait(&ctl.pv_done, (t - 1) & 1, &ctl.abort, a.status);
+      // P^T(t) reuses the buffer PV(t-2) read; a rescale of O^T also needs
+      // PV(t-1) to be complete.
+      if (t >= 2 && !my_abort)
+        my_abort = !mbar_wait(&ctl.pv_done[t & 1], ((t >> 1) - 1) & 1, &ctl.abort, a.status);
+      if (rescale && !my_abort)
+        my_abort = !mbar_wait(&ctl.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, &ctl.abort, a.status);
+      my_abort = __any_sync(0xffffffffu, my_abort);
       tc::fence_after_sync();
       if (!my_abort && rescale) {
 #pragma unroll 1
-        for (int c = 0; c < NQ / 16; ++c) {
-          bool any = false;
+        for (int m = 0; m < 4; ++m) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) any |= ctl.alpha[16 * c + k] != 1.f;
-          if (!any) continue;
-#pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
-            float v[16];
-            tc::tmem_ld16(t_lane + m * Cfg::kOStride + 16 * c, v);
+          for (int c = 0; c < HC / 8; ++c) {
+            float v[8];
+            tc::tmem_ld8(t_lane + m * Cfg::kOStride + c0 + 8 * c, v);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] *= ctl.alpha[16 * c + k];
-            tc::tmem_st16(t_lane + m * Cfg::kOStride + 16 * c, v);
+            for (int k = 0; k < 8; ++k) v[k] *= ctl.alpha[c0 + 8 * c + k];
+            tc::tmem_st8(t_lane + m * Cfg::kOStride + c0 + 8 * c, v);
           }
         }
         tc::tmem_wait_st();
       }
-
-      // ---- pass 2: P = exp2(s - m) -> bf16 into P^T; residual sums for LSE.
       if (!my_abort) {
-#pragma unroll 1
-        for (int gq = 0; gq < Cfg::kGroups; ++gq) {
-          float v[32];
-          load_group<NQ>(s_addr + 32 * gq, gq, v);
-          const uint32_t vw = gq == 0 ? vis0 : (gq == 1 ? vis1 : vis2);
-          const float* mu = &ctl.muse[32 * gq];
-          const uint32_t prow = pbase + 32 * gq * 128;
+        const uint32_t pb_t = pbase + (t & 1) * Cfg::kPBuf;
+        const float4* mu4 = reinterpret_cast<const float4*>(&ctl.muse[c0]);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            float r = 0.f;
-            if (32 * gq + k < NQ) {
-              const float x = ((vw >> k) & 1u) ? fmaf(v[k], scale, -mu[k]) : -INFINITY;
-              const float p = ex2_approx(x);
-              const __nv_bfloat16 hb = __float2bfloat16_rn(p);
-              const uint16_t hv = *reinterpret_cast<const uint16_t*>(&hb);
-              asm volatile("st.shared.u16 [%0], %1;" ::"r"(prow + k * 128 + ((jc ^ (uint32_t)(k & 7)) << 4)), "h"(hv)
-                           : "memory");
-              r = p - __bfloat162float(hb);
-            }
-            v[k] = r;
-          }
-          const float rs = warp_transpose_reduce<false>(v, lane);
-          if (gq == 0) l_res0 += rs;
-          else if (gq == 1) l_res1 += rs;
-          else l_res2 += rs;
+        for (int k4 = 0; k4 < HC / 4; ++k4) {
+          const float4 mu = mu4[k4];
+          const float p0 = ex2_approx(s[4 * k4 + 0] - mu.x);  // s = -inf (masked) gives 0
+          const float p1 = ex2_approx(s[4 * k4 + 1] - mu.y);
+          const float p2 = ex2_approx(s[4 * k4 + 2] - mu.z);
+          const float p3 = ex2_approx(s[4 * k4 + 3] - mu.w);
+          const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+          const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+          const uint32_t w01 = *reinterpret_cast<const uint32_t*>(&h01);
+          const uint32_t w23 = *reinterpret_cast<const uint32_t*>(&h23);
+          acc_r[4 * k4 + 0] += p0 - __uint_as_float(w01 << 16);
+          acc_r[4 * k4 + 1] += p1 - __uint_as_float(w01 & 0xFFFF0000u);
+          acc_r[4 * k4 + 2] += p2 - __uint_as_float(w23 << 16);
+          acc_r[4 * k4 + 3] += p3 - __uint_as_float(w23 & 0xFFFF0000u);
+          const int k = 4 * k4;
+          asm volatile(
+              "st.shared.u16 [%0], %4;\n\tst.shared.u16 [%1], %5;\n\tst.shared.u16 [%2], %6;\n\tst.shared.u16 [%3], %7;" ::"r"(
+                  pb_t + (k + 0) * 128 + ((jc ^ (uint32_t)((k + 0) & 7)) << 4)),
+              "r"(pb_t + (k + 1) * 128 + ((jc ^ (uint32_t)((k + 1) & 7)) << 4)),
+              "r"(pb_t + (k + 2) * 128 + ((jc ^ (uint32_t)((k + 2) & 7)) << 4)),
+              "r"(pb_t + (k + 3) * 128 + ((jc ^ (uint32_t)((k + 3) & 7)) << 4)), "h"((uint16_t)(w01 & 0xFFFFu)),
+              "h"((uint16_t)(w01 >> 16)), "h"((uint16_t)(w23 & 0xFFFFu)), "h"((uint16_t)(w23 >> 16))
+              : "memory");
         }
       }
-      // The scores of this tile are no longer needed, nor (after the MMA reads
-      // it) P^T; hand the S^T buffer back and P^T to the MMA.
-      tc::fence_before_sync();
       fence_proxy_async_smem();
+      tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0 && !my_abort) {
-        mbar_arrive(&ctl.s_free[sb]);
-        mbar_arrive(&ctl.p_full);
-      }
-      // Column sums of this tile's bf16 P (the MMA reads P^T concurrently).
+      if (lane == 0 && !my_abort) mbar_arrive(&ctl.p_full);
+      // bf16 column sums of this tile (the MMA reads P^T concurrently).  The
+      // chunk order is staggered by column so the 8 threads of a bank group
+      // read 8 different 16-byte chunks.
       named_bar_sync(1, kSoftmaxThreads);
-      if (tid < NQ && !my_abort) {
-        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          const int c = (k + tid) & 7;  // staggered: 8 neighbouring rows hit 8 different chunks
-          const uint32_t addr = sP + (k >> 3) * Cfg::kPRegion + tid * 128 + c * 16;
+      if (tid < 2 * NQ && !my_abort) {
+        const int col = tid >> 1;
+        const uint32_t row = sP + (t & 1) * Cfg::kPBuf + (tid & 1) * Cfg::kPRegion + col * 128;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
           uint32_t w0, w1, w2, w3;
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3) : "r"(addr));
-          acc0 += __uint_as_float(w0 << 16) + __uint_as_float(w1 << 16) + __uint_as_float(w2 << 16) +
-                  __uint_as_float(w3 << 16);
-          acc1 += __uint_as_float(w0 & 0xFFFF0000u) + __uint_as_float(w1 & 0xFFFF0000u) +
-                  __uint_as_float(w2 & 0xFFFF0000u) + __uint_as_float(w3 & 0xFFFF0000u);
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                       : "r"(row + (((k + col) & 7) << 4)));
+          a0 += (__uint_as_float(w0 << 16) + __uint_as_float(w1 << 16)) +
+                (__uint_as_float(w2 << 16) + __uint_as_float(w3 << 16));
+          a1 += (__uint_as_float(w0 & 0xFFFF0000u) + __uint_as_float(w1 & 0xFFFF0000u)) +
+                (__uint_as_float(w2 & 0xFFFF0000u) + __uint_as_float(w3 & 0xFFFF0000u));
         }
-        l_col += acc0 + acc1;
+        l_half += a0 + a1;
       }
     }
 
-    // ---- epilogue: O = O^T / l, LSE -------------------------------------------
-    if (!my_abort) my_abort = !mbar_wait(&ctl.pv_done, (nt - 1) & 1, &ctl.abort, a.status);
+    // ---- epilogue: l, LSE, O = O^T / l ----------------------------------------
+    if (!my_abort) my_abort = !mbar_wait(&ctl.pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, &ctl.abort, a.status);
     tc::fence_after_sync();
     const bool wa = __any_sync(0xffffffffu, my_abort) || ctl.abort;
     if (lane == 0) ctl.flag[nt & 1][warp] = wa ? 2 : 0;
-    if (lane < NQ) ctl.red[warp][lane] = l_res0;
-    if (32 + lane < NQ) ctl.red[warp][32 + lane] = l_res1;
-    if (64 + lane < NQ) ctl.red[warp][64 + lane] = l_res2;
+    if (tid < 2 * NQ) ctl.red[tid & 1][tid >> 1] = l_half;
+    warp_columns_to_smem<HC, false>(acc_r, &ctl.red2[quad][c0], lane);
     named_bar_sync(1, kSoftmaxThreads);
-    const int f = ctl.flag[nt & 1][0] | ctl.flag[nt & 1][1] | ctl.flag[nt & 1][2] | ctl.flag[nt & 1][3];
+    int f = 0;
+#pragma unroll
+    for (int w = 0; w < kSoftmaxWarps; ++w) f |= ctl.flag[nt & 1][w];
     if (tid < NQ) {
-      const float lfull = l_col + ((ctl.red[0][tid] + ctl.red[1][tid]) + (ctl.red[2][tid] + ctl.red[3][tid]));
-      ctl.alpha[tid] = l_col > 0.f ? 1.f / l_col : 0.f;
+      const float lp = ctl.red[0][tid] + ctl.red[1][tid];
+      const float lr = (ctl.red2[0][tid] + ctl.red2[1][tid]) + (ctl.red2[2][tid] + ctl.red2[3][tid]);
+      ctl.alpha[tid] = lp > 0.f ? 1.f / lp : 0.f;
       if (!(f & 2) && tid < nrows)
-        lse_out[tid] = l_col > 0.f ? (ctl.muse[tid] + __log2f(lfull)) * 0.69314718055994530942f : -INFINITY;
+        lse_out[tid] = lp > 0.f ? (ctl.muse[tid] + __log2f(lp + lr)) * 0.69314718055994530942f : -INFINITY;
     }
     named_bar_sync(1, kSoftmaxThreads);
     if (!(f & 2)) {
-      float* po = a.part_o + ((int64_t)s_idx * a.rows_max + grow0) * kDLatent + j;
+      // Stage O rows (fp32, 2 KB each) over the now idle Q / P^T / ring space.
+      float* stage = reinterpret_cast<float*>(smem);
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
-#pragma unroll 1
-        for (int c = 0; c < NQ / 16; ++c) {
-          float v[16];
-          tc::tmem_ld16(t_lane + m * Cfg::kOStride + 16 * c, v);
-          tc::tmem_wait_ld();
-          const float* inv = &ctl.alpha[16 * c];
-          float* dst = po + (int64_t)(16 * c) * kDLatent + 128 * m;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            if (16 * c + k < nrows && inv[k] > 0.f) dst[(int64_t)k * kDLatent] = v[k] * inv[k];
+        for (int c = 0; c < HC / 8; ++c) {
+          float v[8];
+          tc::tmem_ld8(t_lane + m * Cfg::kOStride + c0 + 8 * c, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int n = c0 + 8 * c + k;
+            stage[n * kDLatent + 128 * m + j] = v[k] * ctl.alpha[n];
           }
         }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, kSoftmaxThreads);
+      if (tid < nrows && ctl.alpha[tid] > 0.f) {
+        tma::store_bulk(a.part_o + ((int64_t)s_idx * a.rows_max + grow0 + tid) * kDLatent, sbase + tid * 2048, 2048);
+        tma::store_commit();
+        tma::store_wait_read();
       }
     }
     tc::fence_before_sync();
@@ -611,12 +624,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) split_tc_kernel(SplitArgs a) {
 }
 
 template <int NQ>
-cudaError_t launch_split_tc_nq(const SplitArgs& a, dim3 grid, cudaStream_t stream) {
+cudaError_t launch_split_tc_nq(const SplitArgs& a, const TcMaps& maps, dim3 grid, cudaStream_t stream) {
   constexpr int smem = tc_smem_bytes<NQ>();
   static_assert(smem <= 232448, "shared memory budget exceeded");
   cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  split_tc_kernel<NQ><<<grid, kTcThreads, smem, stream>>>(a);
+  split_tc_kernel<NQ><<<grid, TcCfg<NQ>::kThreads, smem, stream>>>(a, maps);
   return cudaGetLastError();
 }
 

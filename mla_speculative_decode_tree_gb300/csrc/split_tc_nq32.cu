@@ -2,8 +2,8 @@
 #include "split_tc.cuh"
 
 namespace mlav {
-cudaError_t launch_split_tc_32(const SplitArgs& a, dim3 grid, cudaStream_t stream) {
-  return launch_split_tc_nq<32>(a, grid, stream);
+cudaError_t launch_split_tc_32(const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t stream) {
+  return launch_split_tc_nq<32>(a, m, grid, stream);
 }
 int split_tc_smem_32() { return tc_smem_bytes<32>(); }
 }  // namespace mlav

@@ -192,20 +192,22 @@ def test_row_selection_and_mask_decoding_exact(H, T, prefixes, flags):
             assert np.array_equal(got, want), (q, h)
 
 
-def test_bad_row_sets_status_and_reads_zero():
+def test_bad_row_sets_status_and_is_excluded():
+    """A key whose pool row is outside the pool is left out (as if masked) and flagged."""
     from oracle import ref
     wl = W.tiny_workload(B=2, H=16, T=4, prefix_lens=[200, 150], pool_rows=1024, seed=5)
     bad = wl["kv_indices"].copy()
-    bad[17] = 5000  # outside the pool
-    wl_bad = dict(wl, kv_indices=bad)
-    o, lse, st, _ = gpu_run(wl_bad)
-    assert st & B.MLA_VERIFY_DEV_BAD_ROW
-    # Reference: the same index pointing at an all-zero row.
-    pool_z = np.concatenate([wl["pool"], np.zeros((1, 576), np.uint16)])
-    ref_idx = bad.copy()
-    ref_idx[17] = 1024
-    o_ref, lse_ref = ref.verify(dict(wl, pool=pool_z, pool_rows=1025, kv_indices=ref_idx), nthreads=NTHREADS)
-    compare(o, lse, o_ref, lse_ref, "bad row")
+    bad[17] = 5000  # request 0, prefix key 17
+    for flags in (0, B.MLA_VERIFY_FORCE_SIMT):
+        o, lse, st, _ = gpu_run(dict(wl, kv_indices=bad), flags=flags)
+        assert st & B.MLA_VERIFY_DEV_BAD_ROW
+        # reference: the same call with key 17 of request 0 masked for every token
+        L = 204
+        bits = np.unpackbits(wl["custom_mask"], bitorder="little").astype(bool)
+        for i in range(4):
+            bits[i * L + 17] = False
+        o_ref, lse_ref = ref.verify(dict(wl, custom_mask=W.pack_bits_lsb(bits)), nthreads=NTHREADS)
+        compare(o, lse, o_ref, lse_ref, "bad row, flags=%d" % flags)
     # the status word is cleared by the read
     o2, lse2, st2, _ = gpu_run(wl)
     assert st2 == 0
