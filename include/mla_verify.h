@@ -179,6 +179,34 @@ int mla_verify_workspace_init(mla_verify_plan_t plan, void* workspace, size_t wo
 int mla_verify_read_status(mla_verify_plan_t plan, void* workspace, void* stream,
                            uint32_t* device_status);
 
+/*
+ * mla_verify_run without a workspace argument, for callers that have no way
+ * to obtain device memory of their own: for example a plugin host that hands
+ * a kernel only its input and output buffers, or a latency-critical path that
+ * must not call cudaMalloc (it can synchronise the device and fail under
+ * memory pressure).  The pages describe nothing like it; it exists for such
+ * integrations.
+ *
+ * The split partials go to a scratch array of 32 MiB compiled into the
+ * library, which every GPU that loads the library keeps reserved until the
+ * process exits.  A plan whose workspace_bytes exceeds 32 MiB is rejected
+ * with MLA_VERIFY_EWORKSPACE (e.g. 64 heads x 9 draft tokens fit up to
+ * nsplit = 28 at batch 1).  Nothing is allocated: the first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress, with that device
+ * current), so make that first call outside any stream capture.  Each call
+ * zeroes the array's 256-byte status header on `stream` and then runs exactly
+ * mla_verify_run on it.  All calls in the process share the one array: calls
+ * whose work overlaps on the GPU (other streams, other threads) race and
+ * corrupt each other's results; serialise them.  Device-detected conditions
+ * are not reported (there is no workspace to read a status word from).
+ * Arguments and errors otherwise as mla_verify_run.
+ */
+int mla_verify_run_noalloc(mla_verify_plan_t plan, const void* q_nope_absorbed, const void* q_rope,
+                           const void* kv_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
+                           const int32_t* out_cache_loc, const uint8_t* custom_mask,
+                           const int32_t* mask_indptr, int32_t batch, float sm_scale, int32_t nsplit,
+                           void* o, float* lse, void* stream);
+
 /* Free the plan (NULL is accepted).  Returns MLA_VERIFY_OK. */
 int mla_verify_destroy(mla_verify_plan_t plan);
 

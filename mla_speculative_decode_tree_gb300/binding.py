@@ -26,7 +26,7 @@ MLA_VERIFY_FORCE_SIMT = 0x1
 
 EXPORTED = ("mla_verify_plan", "mla_verify_plan_describe", "mla_verify_run", "mla_verify_split",
             "mla_verify_merge", "mla_verify_workspace_init", "mla_verify_read_status", "mla_verify_destroy",
-            "mla_verify_strerror")
+            "mla_verify_strerror", "mla_verify_run_noalloc")
 
 
 class MlaVerifyParams(ctypes.Structure):
@@ -67,6 +67,7 @@ def load(path: str = LIB_PATH):
     lib.mla_verify_run.argtypes = run_args + [P, P, P]
     lib.mla_verify_split.argtypes = run_args + [P]
     lib.mla_verify_merge.argtypes = [P, i32, i32, P, sz, P, P, P]
+    lib.mla_verify_run_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, i32, f32, i32, P, P, P]
     lib.mla_verify_workspace_init.argtypes = [P, P, sz, P]
     lib.mla_verify_read_status.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_verify_destroy.argtypes = [P]
@@ -168,6 +169,16 @@ def mla_verify_split(plan: Plan, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv
                                  _ptr(mask_indptr), int(batch), float(sm_scale), int(nsplit), _ptr(workspace),
                                  int(ws_bytes), _stream(stream))
     _check(rc, "mla_verify_split")
+
+
+def mla_verify_run_noalloc(plan: Plan, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, out_cache_loc,
+                           custom_mask, mask_indptr, batch: int, sm_scale: float, nsplit: int, o, lse, stream=None):
+    """mla_verify_run on the library's built-in scratch array (no workspace, no allocation)."""
+    rc = load().mla_verify_run_noalloc(ctypes.c_void_p(plan.handle), _ptr(q_nope_absorbed), _ptr(q_rope),
+                                       _ptr(kv_pool), _ptr(kv_indptr), _ptr(kv_indices), _ptr(out_cache_loc),
+                                       _ptr(custom_mask), _ptr(mask_indptr), int(batch), float(sm_scale), int(nsplit),
+                                       _ptr(o), _ptr(lse), _stream(stream))
+    _check(rc, "mla_verify_run_noalloc")
 
 
 def mla_verify_merge(plan: Plan, batch: int, nsplit: int, workspace, o, lse, stream=None,

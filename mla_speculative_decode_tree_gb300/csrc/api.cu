@@ -156,6 +156,12 @@ int check_common(const mla_verify_plan_s* pl, int32_t batch, int32_t nsplit, voi
 
 }  // namespace
 
+namespace mlav {
+// Records the text of a CUDA error for mla_verify_strerror (used by other
+// translation units of the library) and returns MLA_VERIFY_ECUDA.
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+}  // namespace mlav
+
 extern "C" {
 
 int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, mla_verify_plan_t* out) {

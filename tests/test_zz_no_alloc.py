@@ -1,0 +1,64 @@
+"""mla_verify_run_noalloc: the verify call for callers that cannot allocate
+device memory (they get no workspace of their own), which runs on a scratch
+array built into the library.
+
+Checked through the C ABI against mla_verify_run with a caller-owned
+workspace, on two calls in a row with different inputs (the scratch array
+keeps the first call's contents), within the parity tolerances.  This file
+sorts last so that a run stopping at the first failure has run every other
+test before it.
+"""
+
+import numpy as np
+import pytest
+
+from mla_speculative_decode_tree_gb300 import binding as B
+from mla_speculative_decode_tree_gb300 import workloads as W
+from parity_util import bf16_to_f64, compare
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 32 << 20
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_speculative_decode_tree_gb300 import build
+    build.build()
+
+
+def _outputs(o, lse, n):
+    return bf16_to_f64(o[:n]).reshape(-1, 512), lse[:n].cpu().numpy().astype(np.float64).reshape(-1)
+
+
+def test_noalloc_matches_workspace_call_twice_in_a_row():
+    first = W.tiny_workload(B=2, H=64, T=9, prefix_lens=[3000, 700], pool_rows=16384, seed=41, nsplit=8)
+    second = W.tiny_workload(B=2, H=64, T=9, prefix_lens=[129, 2500], pool_rows=16384, seed=42, nsplit=8)
+    v = B.Verifier(2, 64, 9, 3009, 16384, 8)
+    assert v.plan.workspace_bytes <= SCRATCH_BYTES
+    o_na = torch.empty_like(v.o)
+    lse_na = torch.empty_like(v.lse)
+    for wl in (first, second):
+        d = B.device_inputs(wl)
+        o_ref, lse_ref = v.run(d, 2, wl["sm_scale"])
+        B.mla_verify_run_noalloc(v.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
+                                 d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], 2, wl["sm_scale"], 8,
+                                 o_na, lse_na)
+        torch.cuda.synchronize()
+        n = 2 * 9
+        a_o, a_l = _outputs(o_na, lse_na, n)
+        r_o, r_l = _outputs(o_ref, lse_ref, n)
+        compare(a_o, a_l, r_o, r_l, "noalloc vs workspace, prefix=%s" % list(wl["prefix_lens"]))
+
+
+def test_noalloc_rejects_plans_beyond_the_scratch_size():
+    p = B.mla_verify_plan(1, 64, 9, 100000, 1 << 20, 64)  # 64 splits x 576 rows of partials > 32 MiB
+    assert p.workspace_bytes > SCRATCH_BYTES
+    dummy = torch.zeros(1 << 10, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.MlaVerifyError) as e:
+        B.mla_verify_run_noalloc(p, dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 1, 0.07, 64,
+                                 dummy, dummy)
+    assert e.value.code == B.MLA_VERIFY_EWORKSPACE
