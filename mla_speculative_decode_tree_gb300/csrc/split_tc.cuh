@@ -190,6 +190,12 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     return;
   }
   const int nt = (int)((j1 - j0 + kKeysPerTile - 1) / kKeysPerTile);
+  // Cluster of G CTAs = G row groups of the same split (same keys): each
+  // issues 1/G of every block's gathers, multicast to all of them.  All
+  // early exits above are uniform across such a cluster.
+  const int G = a.cluster;
+  const uint32_t crank = G > 1 ? cluster::ctarank() : 0u;
+  const uint16_t cmask = (uint16_t)((1u << G) - 1u);
   const int i0 = r0 / a.H;
   const int ntok = (r0 + nrows - 1) / a.H - i0 + 1;
 
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
   if (tid == 0) {
     for (int k = 0; k < S; ++k) {
       mbar_init(&ctl.full[k], 1);
-      mbar_init(&ctl.empty[k], 1);
+      mbar_init(&ctl.empty[k], G);  // one release per CTA of the cluster
     }
     mbar_init(&ctl.q_full, 1);
     mbar_init(&ctl.s_full, 1);
@@ -239,6 +245,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
+  if (G > 1) cluster::sync();  // peers' barriers exist before any multicast reaches them
   tc::fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
 
@@ -276,10 +283,14 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         return;
       }
       if (blk >= 0) {
+        // the slot fills with all 32 gathers of the block, from every CTA
         if (lane == 0) tma::arrive_expect_tx(&ctl.full[slot], Cfg::kSlotBytes);
         __syncwarp();
-        tma::gather4(sRing + slot * Cfg::kSlotBytes + lane * 512, &maps.kv, blk * 64, r[0], r[1], r[2], r[3],
-                     &ctl.full[slot]);
+        const uint32_t dst = sRing + slot * Cfg::kSlotBytes + lane * 512;
+        if (G == 1)
+          tma::gather4(dst, &maps.kv, blk * 64, r[0], r[1], r[2], r[3], &ctl.full[slot]);
+        else if (lane % G == (int)crank)
+          tma::gather4_multicast(dst, &maps.kv, blk * 64, r[0], r[1], r[2], r[3], &ctl.full[slot], cmask);
       } else if (lane == 0) {
         mbar_arrive(&ctl.full[slot]);
       }
@@ -317,6 +328,17 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         }
       }
     }
+    // Tail: wait until every CTA has released this warp's last slots, so no
+    // peer's release can still arrive at this CTA's barriers after it exits.
+    if (!stop) {
+      const int total = seq;
+#pragma unroll 1
+      for (int q = total - S; q < total; ++q) {
+        if (q < 0 || q % Cfg::kProducerWarps != pw) continue;
+        const bool got = mbar_wait(&ctl.empty[q % S], (q / S) & 1, &ctl.abort, a.status);
+        if (!__all_sync(0xffffffffu, got)) break;
+      }
+    }
     if (bad) atomicOr(a.status, kStatusBadRow);
   } else if (warp == kMmaWarp) {
     // ============================ MMA issue ==================================
@@ -330,6 +352,12 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         const bool r = mbar_wait(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
         tc::fence_after_sync();
         return r;
+      };
+      // A slot is free again once the MMAs reading it are done -- in every
+      // CTA of the cluster, since the next fill is multicast to all of them.
+      auto release = [&](int slot) {
+        if (G == 1) tc::mma_commit(&ctl.empty[slot]);
+        else tc::mma_commit_multicast(&ctl.empty[slot], cmask);
       };
 #pragma unroll 1
       for (int t = 0; t <= nt && ok; ++t) {
@@ -351,7 +379,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
               const uint64_t bdesc = tc::smem_desc(sQ + blk * Cfg::kQBlock + k * 32, 16, 1024, tc::kSwizzle128B);
               tc::mma_bf16_ss(tmem + Cfg::kColS, adesc, bdesc, idesc_qk, (blk | k) ? 1u : 0u);
             }
-            tc::mma_commit(&ctl.empty[slot]);
+            release(slot);
           }
           if (!ok) break;
           tc::mma_commit(&ctl.s_full);
@@ -366,7 +394,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
             int sa, sb;
             if (seq % S == S - 1) {
               if (!(ok = take(sa))) break;
-              mbar_arrive(&ctl.empty[sa]);
+              release(sa);
               ++seq;
             }
             if (!(ok = take(sa))) break;
@@ -382,8 +410,8 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
                                 tc::kSwizzle128B);
               tc::mma_bf16_ss(tmem + m * Cfg::kOStride, adesc, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
             }
-            tc::mma_commit(&ctl.empty[sa]);
-            tc::mma_commit(&ctl.empty[sb]);
+            release(sa);
+            release(sb);
           }
           if (ok) tc::mma_commit(&ctl.pv_done[u & 1]);
         }
@@ -621,6 +649,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
+  if (G > 1) cluster::sync();  // no peer still writes into this CTA's shared memory
 }
 
 template <int NQ>
@@ -629,7 +658,20 @@ cudaError_t launch_split_tc_nq(const SplitArgs& a, const TcMaps& maps, dim3 grid
   static_assert(smem <= 232448, "shared memory budget exceeded");
   cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  split_tc_kernel<NQ><<<grid, TcCfg<NQ>::kThreads, smem, stream>>>(a, maps);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(TcCfg<NQ>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.cluster > 1 ? a.cluster : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, split_tc_kernel<NQ>, a, maps);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
