@@ -73,8 +73,7 @@ extern "C" {
 #define MLA_VERIFY_DEV_TIMEOUT 0x2u /* a pipeline wait gave up; that CTA's partial is invalid */
 
 /* Plan flags. */
-#define MLA_VERIFY_FORCE_SIMT 0x1   /* use the CUDA-core (warp-shuffle) split kernel for every shape */
-#define MLA_VERIFY_NO_MULTICAST 0x2 /* tensor-core kernel: each CTA gathers its own rows (no clusters) */
+#define MLA_VERIFY_FORCE_SIMT 0x1 /* use the CUDA-core (warp-shuffle) split kernel for every shape */
 
 typedef struct mla_verify_plan_s* mla_verify_plan_t; /* opaque, host-only, immutable after plan */
 
@@ -87,7 +86,7 @@ typedef struct {
   int32_t nsplit;     /* >= 1: KV chunks per request = partials per output row (fixed grid dimension) */
   int32_t d_latent;   /* must be 512 */
   int32_t d_rope;     /* must be 64 */
-  int32_t flags;      /* MLA_VERIFY_FORCE_SIMT, MLA_VERIFY_NO_MULTICAST, or 0 */
+  int32_t flags;      /* MLA_VERIFY_FORCE_SIMT or 0 */
 } mla_verify_params;
 
 /* What a plan chose (for tests, benchmarks and logs). */
@@ -99,7 +98,6 @@ typedef struct {
   int32_t merge_blocks;  /* merge grid size */
   int32_t smem_bytes;    /* dynamic shared memory of the split kernel */
   size_t workspace_bytes;
-  int32_t cluster;       /* CTAs (row groups of one split) that share each gathered row by TMA multicast */
 } mla_verify_plan_info;
 
 /*

@@ -23,7 +23,6 @@ MLA_VERIFY_ECUDA = 4
 MLA_VERIFY_DEV_BAD_ROW = 0x1
 MLA_VERIFY_DEV_TIMEOUT = 0x2
 MLA_VERIFY_FORCE_SIMT = 0x1
-MLA_VERIFY_NO_MULTICAST = 0x2
 
 EXPORTED = ("mla_verify_plan", "mla_verify_plan_describe", "mla_verify_run", "mla_verify_split",
             "mla_verify_merge", "mla_verify_workspace_init", "mla_verify_read_status", "mla_verify_destroy",
@@ -40,7 +39,7 @@ class MlaVerifyPlanInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32), ("keys_per_tile", ctypes.c_int32),
                 ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),
                 ("merge_blocks", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t), ("cluster", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 class MlaVerifyError(RuntimeError):

@@ -23,7 +23,6 @@ struct mla_verify_plan_s {
   size_t off_lse, off_o, ws_bytes;
   int merge_blocks;
   int smem;
-  int cluster;  // row groups of one split sharing gathered rows by TMA multicast
 };
 
 namespace {
@@ -172,7 +171,7 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
       p.pool_rows < 1 || p.max_kv_len < p.q_len)
     return MLA_VERIFY_EINVAL;
   if (p.d_latent != kDLatent || p.d_rope != kDRope) return MLA_VERIFY_EUNSUPPORTED;
-  if ((p.flags & ~(MLA_VERIFY_FORCE_SIMT | MLA_VERIFY_NO_MULTICAST)) != 0) return MLA_VERIFY_EINVAL;
+  if ((p.flags & ~MLA_VERIFY_FORCE_SIMT) != 0) return MLA_VERIFY_EINVAL;
   const int64_t rows_b = (int64_t)p.q_len * p.num_heads;
   const int64_t rows_max = rows_b * p.max_batch;
   if (rows_max > (int64_t)1 << 30 || p.pool_rows > ((int64_t)1 << 31) - 1) return MLA_VERIFY_EINVAL;
@@ -187,15 +186,7 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
   pl->nq = pl->kernel ? pick_nq((int)rows_b) : kSimtRowsPerCta;
   pl->groups = (int)((rows_b + pl->nq - 1) / pl->nq);
   pl->smem = pl->kernel ? tc_smem(pl->nq) : 0;
-  // The row groups of a split read the same keys: a cluster of them fetches
-  // each key once (largest divisor of the group count up to 8 CTAs).
-  pl->cluster = 1;
-  if (pl->kernel && !(p.flags & MLA_VERIFY_NO_MULTICAST))
-    for (int c = 8; c >= 2; --c)
-      if (pl->groups % c == 0) {
-        pl->cluster = c;
-        break;
-      }
+
   pl->off_lse = kWsHeader;
   pl->off_o = round_up(pl->off_lse + sizeof(float) * (size_t)p.nsplit * (size_t)rows_max, 256);
   pl->ws_bytes = pl->off_o + sizeof(float) * (size_t)p.nsplit * (size_t)rows_max * kDLatent;
@@ -216,7 +207,6 @@ int mla_verify_plan_describe(mla_verify_plan_t pl, mla_verify_plan_info* info) {
   info->merge_blocks = pl->merge_blocks;
   info->smem_bytes = pl->smem;
   info->workspace_bytes = pl->ws_bytes;
-  info->cluster = pl->cluster;
   return MLA_VERIFY_OK;
 }
 
@@ -252,7 +242,6 @@ int mla_verify_split(mla_verify_plan_t pl, const void* q_nope_absorbed, const vo
   a.pool_rows = pl->p.pool_rows;
   a.rows_max = pl->rows_max;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
-  a.cluster = pl->cluster;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.part_lse = reinterpret_cast<float*>(ws + pl->off_lse);
@@ -273,12 +262,6 @@ int mla_verify_split(mla_verify_plan_t pl, const void* q_nope_absorbed, const vo
         (rc = encode_bf16_2d(enc, &maps.qr, q_rope, kDRope, rows_total, 64, pl->nq)) != MLA_VERIFY_OK)
       return rc;
     e = tc_launch(pl->nq, a, maps, grid, st);
-    if (e != cudaSuccess && a.cluster > 1) {
-      // The device could not co-schedule the cluster: run without multicast.
-      (void)cudaGetLastError();
-      a.cluster = 1;
-      e = tc_launch(pl->nq, a, maps, grid, st);
-    }
   } else {
     e = launch_split_simt(a, grid, st);
   }

@@ -31,7 +31,6 @@ struct SplitArgs {
   const uint8_t* mask;           // packed bits LSB-first
   const int32_t* mask_indptr;    // [B] bit offsets
   int32_t batch, H, T, nsplit;
-  int32_t cluster;               // CTAs (row groups of one split) sharing gathered rows by multicast
   int64_t pool_rows;
   int64_t rows_max;              // max_batch*T*H: row stride of one split's partials
   float scale_log2;              // sm_scale * log2(e): scores are kept in base 2

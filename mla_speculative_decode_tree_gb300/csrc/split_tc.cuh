@@ -24,7 +24,7 @@
 // tile are fetched a second time (after the next tile's key blocks) rather
 // than kept resident: a whole 128-key tile (144 KB) does not fit next to Q.
 //
-// Warp roles (CG = 2 column groups; 32*(4*CG+4) = 384 threads):
+// Warp roles (up to 512 threads; CG = 3 column groups for NQ = 96, else 2):
 //   warps 0..4CG-1  softmax.  Warp w reads TMEM lane quadrant w%4 (keys
 //              32(w%4)..+31 of the tile) and owns query columns
 //              [(w/4)*NQ/CG, (w/4+1)*NQ/CG).  It loads its scores once (the S^T
@@ -37,8 +37,9 @@
 //              rounding residual p - bf16(p) (completes LSE).  Epilogue: O^T
 //              scaled by 1/l into shared memory, bulk-stored as 2 KB rows.
 //   warp 4CG   TMEM allocation and the single MMA-issuing thread.
-//   warps 4CG+1..4CG+3  gather, taking turns block by block: TMA
-//              tile::gather4 of four 128-byte row segments per lane, rows resolved from kv_indices (prefix) or out_cache_loc
+//   warps 4CG+1..  gather (at most one per ring slot), taking turns block by block: cp.async 16-byte
+//              copies (from several warps: a single warp cannot issue them
+//              fast enough), rows resolved from kv_indices (prefix) or out_cache_loc
 //              (drafts) [Capture Safety to MoE Ceiling, §"The Architecture of
 //              Capture Safety"]; Q by 2-D TMA.
 // Block sequence through the ring: K(0), K(1), V(0), K(2), V(1), ...,
@@ -57,18 +58,16 @@
 namespace mlav {
 
 constexpr float kTau = 8.0f;  // base-2 headroom before the running max is raised
+constexpr int kPrefetchTiles = 2;  // tiles of rows pulled into L2 ahead of the ring
 
 template <int NQ>
 struct TcCfg {
   static_assert(NQ % 16 == 0 && NQ >= 16 && NQ <= 96, "NQ must be a multiple of 16 in [16, 96]");
-  static constexpr int kCG = 2;                 // softmax warps per TMEM lane quadrant
+  static constexpr int kCG = NQ == 96 ? 3 : 2;  // softmax warps per TMEM lane quadrant
   static constexpr int kHC = NQ / kCG;          // query columns per softmax thread
   static constexpr int kSoftmaxWarps = 4 * kCG;
   static constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
   static constexpr int kMmaWarp = kSoftmaxWarps;
-  static constexpr int kProducerWarp = kSoftmaxWarps + 1;  // first of kProducerWarps gather warps
-  static constexpr int kProducerWarps = 3;
-  static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kProducerWarps);
   static_assert(kHC % 8 == 0, "columns per softmax thread must be a multiple of 8");
   static constexpr int kQBlock = NQ * 128;  // one 64-column block of Q
   static constexpr int kQBytes = 9 * kQBlock;
@@ -82,6 +81,14 @@ struct TcCfg {
   static constexpr int kOffCtl = kOffRing + kStages * kSlotBytes;
   static constexpr int kOStride = (NQ + 31) / 32 * 32;  // TMEM columns per O^T block (32-aligned)
   static constexpr int kColS = 4 * kOStride;
+  // Gather warps: up to 16 warps in all, and no more than ring slots.  A warp
+  // fills every kProducerWarps-th block; with more warps than slots it could
+  // reach a slot whose empty barrier is two phases behind, where the parity
+  // wait cannot tell the phases apart.
+  static constexpr int kProducerWarp = kSoftmaxWarps + 1;
+  static constexpr int kProducerWarps = (15 - kSoftmaxWarps) < kStages ? (15 - kSoftmaxWarps) : kStages;
+  static_assert(kProducerWarps >= 1 && kProducerWarps <= kStages, "gather warps must not outnumber ring slots");
+  static constexpr int kThreads = 32 * (kProducerWarp + kProducerWarps);
   static_assert(NQ * 2048 <= kOffCtl, "epilogue staging must fit below the control block");
 };
 
@@ -190,12 +197,6 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     return;
   }
   const int nt = (int)((j1 - j0 + kKeysPerTile - 1) / kKeysPerTile);
-  // Cluster of G CTAs = G row groups of the same split (same keys): each
-  // issues 1/G of every block's gathers, multicast to all of them.  All
-  // early exits above are uniform across such a cluster.
-  const int G = a.cluster;
-  const uint32_t crank = G > 1 ? cluster::ctarank() : 0u;
-  const uint16_t cmask = (uint16_t)((1u << G) - 1u);
   const int i0 = r0 / a.H;
   const int ntok = (r0 + nrows - 1) / a.H - i0 + 1;
 
@@ -210,8 +211,8 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
   // ---- set-up ---------------------------------------------------------------
   if (tid == 0) {
     for (int k = 0; k < S; ++k) {
-      mbar_init(&ctl.full[k], 1);
-      mbar_init(&ctl.empty[k], G);  // one release per CTA of the cluster
+      mbar_init(&ctl.full[k], 32);  // every lane of the filling warp
+      mbar_init(&ctl.empty[k], 1);
     }
     mbar_init(&ctl.q_full, 1);
     mbar_init(&ctl.s_full, 1);
@@ -245,27 +246,32 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (G > 1) cluster::sync();  // peers' barriers exist before any multicast reaches them
   tc::fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
 
   if (warp >= kProducerWarp) {
     // =========================== gather ======================================
-    // The producer warps walk the same block sequence and take turns: warp pw
-    // issues the blocks with seq % kProducerWarps == pw (one warp alone cannot
-    // issue row gathers fast enough to keep the tensor cores fed).
+    // The gather warps walk the same block sequence and take turns: warp pw
+    // fills the blocks with seq % kProducerWarps == pw.  A block is 128 keys x
+    // 64 columns: lane (jl = lane/8, c = lane%8) copies 16-byte chunk c of
+    // keys 4*it + jl, it = 0..31, into its swizzled place (cp.async, L2 only);
+    // the copies of a lane signal full[slot] when they land.
     const int pw = warp - kProducerWarp;
+    const int jl = lane >> 3, c8 = lane & 7;
     if (pw == 0 && lane == 0) {
       tma::arrive_expect_tx(&ctl.q_full, 9 * Cfg::kQBlock);
 #pragma unroll 1
       for (int blk = 0; blk < 8; ++blk) tma::load_2d(sQ + blk * Cfg::kQBlock, &maps.qn, blk * 64, (int)grow0, &ctl.q_full);
       tma::load_2d(sQ + 8 * Cfg::kQBlock, &maps.qr, 0, (int)grow0, &ctl.q_full);
     }
-    // Keys past the split's end or resolving outside the pool are fetched
-    // from the split's first row (finite by contract); the softmax masks them.
+    // Row ids: lane (jl, c8) resolves keys 4*(c8 + 8m) + jl, m = 0..3, which
+    // are exactly the keys lanes 8*jl.. copy at iterations it = c8 + 8m; a
+    // shuffle of own[it/8] from lane 8*jl + it%8 hands each copier its row.
+    // Keys past the split's end or resolving outside the pool are fetched from
+    // the split's first row (finite by contract); the softmax masks them.
     int64_t rsub = resolve_row(a, b, P, kv_base, j0);
     if (rsub < 0) rsub = 0;
-    int rows[4] = {0, 0, 0, 0}, prev[4] = {0, 0, 0, 0};
+    int own[4] = {0, 0, 0, 0}, prev[4] = {0, 0, 0, 0};
     uint32_t bad = 0;
     int seq = 0;
     bool stop = false;
@@ -283,26 +289,44 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         return;
       }
       if (blk >= 0) {
-        // the slot fills with all 32 gathers of the block, from every CTA
-        if (lane == 0) tma::arrive_expect_tx(&ctl.full[slot], Cfg::kSlotBytes);
-        __syncwarp();
-        const uint32_t dst = sRing + slot * Cfg::kSlotBytes + lane * 512;
-        if (G == 1)
-          tma::gather4(dst, &maps.kv, blk * 64, r[0], r[1], r[2], r[3], &ctl.full[slot]);
-        else if (lane % G == (int)crank)
-          tma::gather4_multicast(dst, &maps.kv, blk * 64, r[0], r[1], r[2], r[3], &ctl.full[slot], cmask);
-      } else if (lane == 0) {
+        const uint32_t base = sRing + slot * Cfg::kSlotBytes + jl * 128;
+        const __nv_bfloat16* src0 = a.kv_pool + blk * 64 + c8 * 8;
+#pragma unroll
+        for (int it = 0; it < 32; ++it) {
+          const int row = __shfl_sync(0xffffffffu, r[it >> 3], 8 * jl + (it & 7));
+          const int swz = (c8 ^ (4 * (it & 1) + jl)) << 4;  // key (4*it + jl) mod 8 = 4*(it%2) + jl
+          cp_async16(base + it * 512 + swz, src0 + (int64_t)row * kDRow, 16u);
+        }
+        cp_async_arrive(&ctl.full[slot]);
+      } else {
         mbar_arrive(&ctl.full[slot]);
       }
       ++seq;
     };
+    // Whole rows of tiles a few steps ahead are pulled into L2, so the copies
+    // hit L2 (the ring's few slots bound the bytes in flight, so latency
+    // bounds the rate).  Key m of a lane is prefetched by warp m % warps.
+    auto prefetch_tile = [&](int tp) {
+      if (tp >= nt) return;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        if (m % Cfg::kProducerWarps != pw) continue;
+        const int64_t j = j0 + (int64_t)tp * kKeysPerTile + 4 * (c8 + 8 * m) + jl;
+        if (j >= j1) continue;
+        const int64_t rr = resolve_row(a, b, P, kv_base, j);
+        if (rr >= 0) tma::prefetch_l2(a.kv_pool + rr * kDRow, kRowBytes);
+      }
+    };
+#pragma unroll 1
+    for (int tp = 1; tp <= kPrefetchTiles; ++tp) prefetch_tile(tp);
 #pragma unroll 1
     for (int t = 0; t <= nt && !stop; ++t) {
       if (t < nt) {
+        prefetch_tile(t + 1 + kPrefetchTiles);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          prev[q] = rows[q];
-          const int64_t j = j0 + (int64_t)t * kKeysPerTile + 4 * lane + q;
+        for (int m = 0; m < 4; ++m) {
+          prev[m] = own[m];
+          const int64_t j = j0 + (int64_t)t * kKeysPerTile + 4 * (c8 + 8 * m) + jl;
           int64_t rr = rsub;
           if (j < j1) {
             rr = resolve_row(a, b, P, kv_base, j);
@@ -311,34 +335,24 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
               rr = rsub;
             }
           }
-          rows[q] = (int)rr;
+          own[m] = (int)rr;
         }
 #pragma unroll 1
-        for (int blk = 0; blk < 9; ++blk) produce(blk, rows);
+        for (int blk = 0; blk < 9; ++blk) produce(blk, own);
       }
       if (t >= 1) {
-        // value blocks of tile t-1: its rows are in prev[] (or still in rows[]
+        // value blocks of tile t-1: its rows are in prev[] (or still in own[]
         // after the last tile)
         const bool last = (t == nt);
 #pragma unroll 1
         for (int pr = 0; pr < 4; ++pr) {
-          if (seq % S == S - 1) produce(-1, rows);
-          produce(2 * pr, last ? rows : prev);
-          produce(2 * pr + 1, last ? rows : prev);
+          if (seq % S == S - 1) produce(-1, own);
+          produce(2 * pr, last ? own : prev);
+          produce(2 * pr + 1, last ? own : prev);
         }
       }
     }
-    // Tail: wait until every CTA has released this warp's last slots, so no
-    // peer's release can still arrive at this CTA's barriers after it exits.
-    if (!stop) {
-      const int total = seq;
-#pragma unroll 1
-      for (int q = total - S; q < total; ++q) {
-        if (q < 0 || q % Cfg::kProducerWarps != pw) continue;
-        const bool got = mbar_wait(&ctl.empty[q % S], (q / S) & 1, &ctl.abort, a.status);
-        if (!__all_sync(0xffffffffu, got)) break;
-      }
-    }
+    cp_async_wait_all();  // nothing in flight when the CTA exits
     if (bad) atomicOr(a.status, kStatusBadRow);
   } else if (warp == kMmaWarp) {
     // ============================ MMA issue ==================================
@@ -347,18 +361,17 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, NQ, true, false);
       int seq = 0;
       bool ok = mbar_wait(&ctl.q_full, 0, &ctl.abort, a.status);
+      // cp.async writes shared memory through the generic proxy and the MMA
+      // reads it through the async proxy: a proxy fence follows each acquire.
       auto take = [&](int& slot) -> bool {
         slot = seq % S;
         const bool r = mbar_wait(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
+        fence_proxy_async_smem();
         tc::fence_after_sync();
         return r;
       };
-      // A slot is free again once the MMAs reading it are done -- in every
-      // CTA of the cluster, since the next fill is multicast to all of them.
-      auto release = [&](int slot) {
-        if (G == 1) tc::mma_commit(&ctl.empty[slot]);
-        else tc::mma_commit_multicast(&ctl.empty[slot], cmask);
-      };
+      // A slot is free again once the MMAs reading it are done.
+      auto release = [&](int slot) { tc::mma_commit(&ctl.empty[slot]); };
 #pragma unroll 1
       for (int t = 0; t <= nt && ok; ++t) {
         if (t < nt) {
@@ -649,7 +662,6 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
-  if (G > 1) cluster::sync();  // no peer still writes into this CTA's shared memory
 }
 
 template <int NQ>
@@ -663,13 +675,8 @@ cudaError_t launch_split_tc_nq(const SplitArgs& a, const TcMaps& maps, dim3 grid
   cfg.blockDim = dim3(TcCfg<NQ>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.cluster > 1 ? a.cluster : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
   e = cudaLaunchKernelEx(&cfg, split_tc_kernel<NQ>, a, maps);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

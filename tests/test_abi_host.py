@@ -67,7 +67,7 @@ def test_plan_workspace_formula(lib):
     (dict(pool_rows=0), B.MLA_VERIFY_EINVAL),
     (dict(max_kv_len=3), B.MLA_VERIFY_EINVAL),
     (dict(flags=0x100), B.MLA_VERIFY_EINVAL),
-    (dict(flags=0x4), B.MLA_VERIFY_EINVAL),
+    (dict(flags=0x2), B.MLA_VERIFY_EINVAL),
 ])
 def test_plan_rejects(lib, kw, code):
     with pytest.raises(B.MlaVerifyError) as e:
@@ -85,20 +85,17 @@ def test_plan_null_pointers(lib):
     assert lib.mla_verify_destroy(None) == B.MLA_VERIFY_OK
 
 
-@pytest.mark.parametrize("H,T,flags,kernel,nq,cluster", [
-    (64, 9, 0, 1, 96, 6),      # 576 rows -> 6 groups of 96, one cluster per split
-    (64, 9, B.MLA_VERIFY_NO_MULTICAST, 1, 96, 1),
-    (128, 9, 0, 1, 96, 6),     # 12 groups -> clusters of 6
-    (8, 9, 0, 1, 80, 1),       # 72 rows  -> 1 group of 80
-    (16, 4, 0, 1, 64, 1),      # 64 rows
-    (8, 1, 0, 0, 8, 1),        # decode with 8 heads: tile mostly padding -> CUDA cores
-    (64, 9, B.MLA_VERIFY_FORCE_SIMT, 0, 8, 1),
+@pytest.mark.parametrize("H,T,flags,kernel,nq", [
+    (64, 9, 0, 1, 96),      # 576 rows -> 6 groups of 96
+    (8, 9, 0, 1, 80),       # 72 rows  -> 1 group of 80
+    (16, 4, 0, 1, 64),      # 64 rows
+    (8, 1, 0, 0, 8),        # decode with 8 heads: tile mostly padding -> CUDA cores
+    (64, 9, B.MLA_VERIFY_FORCE_SIMT, 0, 8),
 ])
-def test_plan_kernel_choice(lib, H, T, flags, kernel, nq, cluster):
+def test_plan_kernel_choice(lib, H, T, flags, kernel, nq):
     info = plan(num_heads=H, q_len=T, max_kv_len=5000 + T, flags=flags).describe()
     assert info.kernel == kernel
     assert info.rows_per_cta == nq
-    assert info.cluster == cluster
     assert info.grid_x == -(-(H * T) // nq)
     assert info.grid_y == 16 and info.grid_z == 1
     if kernel:

@@ -76,8 +76,7 @@ ADHOC = [
 ]
 
 
-@pytest.mark.parametrize("flags", [0, B.MLA_VERIFY_FORCE_SIMT, B.MLA_VERIFY_NO_MULTICAST],
-                         ids=["auto", "simt", "nomc"])
+@pytest.mark.parametrize("flags", [0, B.MLA_VERIFY_FORCE_SIMT], ids=["auto", "simt"])
 @pytest.mark.parametrize("case", ADHOC, ids=[str(i) for i in range(len(ADHOC))])
 def test_parity_adhoc(case, flags):
     Bn, H, T, prefixes, pool, nsplit, tree = case
@@ -110,17 +109,6 @@ def test_parity_full_configs_sampled(name):
     if name == "needle64k":
         assert np.abs(o_ref).max() > 1.0  # the planted keys really dominate
     print(name, v.plan.describe().kernel, err)
-
-
-@pytest.mark.slow
-def test_mid64k_multicast_matches_per_cta_gather():
-    """Clusters sharing rows by multicast give the same bits as per-CTA gathers."""
-    wl = full_workload("mid64k")
-    o1, lse1, st1, v1 = gpu_run(wl)
-    o2, lse2, st2, v2 = gpu_run(wl, flags=B.MLA_VERIFY_NO_MULTICAST)
-    assert v1.plan.describe().cluster == 6 and v2.plan.describe().cluster == 1
-    assert st1 == 0 and st2 == 0
-    assert np.array_equal(o1, o2) and np.array_equal(lse1, lse2)
 
 
 @pytest.mark.slow
