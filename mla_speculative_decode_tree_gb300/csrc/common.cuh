@@ -41,7 +41,7 @@ struct SplitArgs {
 
 // TMA descriptors of one call: the pool for row gathers (box 64 columns x 1
 // row, 128-byte swizzle) and the two query tensors (box 64 columns x NQ rows).
-struct alignas(64) TcMaps {
+struct TcMaps {  // CUtensorMap carries its own (64-byte or larger) alignment
   CUtensorMap kv, qn, qr;
 };
 
@@ -154,6 +154,12 @@ __device__ __forceinline__ int64_t resolve_row(const SplitArgs& a, int b, int64_
   int64_t r = (j < P) ? (int64_t)__ldg(a.kv_indices + kv_base + j)
                       : (int64_t)__ldg(a.out_cache_loc + (int64_t)b * a.T + (j - P));
   return (r >= 0 && r < a.pool_rows) ? r : -1;
+}
+
+// The raw index entry of key position j (no range check): lets a caller issue
+// the load early and check it when the value is used.
+__device__ __forceinline__ int32_t load_row_id(const SplitArgs& a, int b, int64_t P, int64_t kv_base, int64_t j) {
+  return (j < P) ? __ldg(a.kv_indices + kv_base + j) : __ldg(a.out_cache_loc + (int64_t)b * a.T + (j - P));
 }
 
 __device__ __forceinline__ uint32_t mask_bit(const uint8_t* mask, int64_t bit) {

@@ -15,8 +15,8 @@
 // to 32, S^T at [4*S_o, 4*S_o + NQ).
 //
 // Shared memory holds Q (9 blocks of NQ rows x 64 columns, 128-byte
-// swizzled, K-major), two P^T buffers (NQ rows x 128 keys, K-major; tile t
-// writes buffer t%2 while the MMA may still read the other) and a ring of 16 KB
+// swizzled, K-major), P^T (NQ rows x 128 keys, K-major; tile t writes it once
+// the MMA of tile t-1 has read it) and a ring of 16 KB
 // slots, each 128 keys x 64 columns of the gathered pool rows in the
 // 128-byte-swizzle atom (8 keys x 128 bytes).  That atom is at once the
 // K-major layout of the key operand and the MN-major layout of the value
@@ -58,7 +58,6 @@
 namespace mlav {
 
 constexpr float kTau = 8.0f;  // base-2 headroom before the running max is raised
-constexpr int kPrefetchTiles = 2;  // tiles of rows pulled into L2 ahead of the ring
 
 template <int NQ>
 struct TcCfg {
@@ -72,10 +71,9 @@ struct TcCfg {
   static constexpr int kQBlock = NQ * 128;  // one 64-column block of Q
   static constexpr int kQBytes = 9 * kQBlock;
   static constexpr int kPRegion = NQ * 128;  // P^T keys 0..63 or 64..127
-  static constexpr int kPBuf = 2 * kPRegion;  // one P^T buffer; two alternate by tile
-  static constexpr int kPBytes = 2 * kPBuf;
+  static constexpr int kPBytes = 2 * kPRegion;
   static constexpr int kSlotBytes = 128 * 128;
-  static constexpr int kStages = NQ >= 96 ? 4 : NQ >= 80 ? 5 : NQ >= 64 ? 7 : NQ >= 48 ? 8 : NQ >= 32 ? 10 : 12;
+  static constexpr int kStages = NQ >= 96 ? 5 : NQ >= 80 ? 6 : NQ >= 64 ? 8 : NQ >= 48 ? 9 : NQ >= 32 ? 11 : 12;
   static constexpr int kOffP = kQBytes;
   static constexpr int kOffRing = kQBytes + kPBytes;
   static constexpr int kOffCtl = kOffRing + kStages * kSlotBytes;
@@ -199,6 +197,14 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
   const int nt = (int)((j1 - j0 + kKeysPerTile - 1) / kKeysPerTile);
   const int i0 = r0 / a.H;
   const int ntok = (r0 + nrows - 1) / a.H - i0 + 1;
+  // The row groups of a split read the same keys; each starts at its own
+  // tile (a rotation of the tile order) so that one group, not all of them at
+  // once, waits on the first fetch of a tile from HBM and the rest find it in
+  // L2.  The order of the tiles does not change the result beyond rounding,
+  // and it is fixed for a given grid.
+  const int groups = (rows_b + NQ - 1) / NQ;
+  const int rot = (int)(((int64_t)g * nt) / groups);
+  auto tile_at = [&](int t) -> int { return t + rot < nt ? t + rot : t + rot - nt; };
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -269,7 +275,24 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     // shuffle of own[it/8] from lane 8*jl + it%8 hands each copier its row.
     // Keys past the split's end or resolving outside the pool are fetched from
     // the split's first row (finite by contract); the softmax masks them.
+    // The index loads run a tile ahead of their use (ids of tile t+1 are
+    // loaded while tile t is fetched), so no gather warp waits on an index
+    // load between tiles.
+    auto key_of = [&](int tile, int m) -> int64_t {
+      return j0 + (int64_t)tile * kKeysPerTile + 4 * (c8 + 8 * m) + jl;
+    };
+    auto load_ids = [&](int t, int (&raw)[4]) {
+      const int tile = tile_at(t < nt ? t : 0);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int64_t j = key_of(tile, m);
+        raw[m] = (t < nt && j < j1) ? load_row_id(a, b, P, kv_base, j) : -1;
+      }
+    };
     int64_t rsub = resolve_row(a, b, P, kv_base, j0);
+    int raw_cur[4], raw_nxt[4];
+    load_ids(0, raw_cur);
+    load_ids(1, raw_nxt);
     if (rsub < 0) rsub = 0;
     int own[4] = {0, 0, 0, 0}, prev[4] = {0, 0, 0, 0};
     uint32_t bad = 0;
@@ -303,40 +326,24 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
       }
       ++seq;
     };
-    // Whole rows of tiles a few steps ahead are pulled into L2, so the copies
-    // hit L2 (the ring's few slots bound the bytes in flight, so latency
-    // bounds the rate).  Key m of a lane is prefetched by warp m % warps.
-    auto prefetch_tile = [&](int tp) {
-      if (tp >= nt) return;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        if (m % Cfg::kProducerWarps != pw) continue;
-        const int64_t j = j0 + (int64_t)tp * kKeysPerTile + 4 * (c8 + 8 * m) + jl;
-        if (j >= j1) continue;
-        const int64_t rr = resolve_row(a, b, P, kv_base, j);
-        if (rr >= 0) tma::prefetch_l2(a.kv_pool + rr * kDRow, kRowBytes);
-      }
-    };
-#pragma unroll 1
-    for (int tp = 1; tp <= kPrefetchTiles; ++tp) prefetch_tile(tp);
 #pragma unroll 1
     for (int t = 0; t <= nt && !stop; ++t) {
       if (t < nt) {
-        prefetch_tile(t + 1 + kPrefetchTiles);
+        const int tile = tile_at(t);
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           prev[m] = own[m];
-          const int64_t j = j0 + (int64_t)t * kKeysPerTile + 4 * (c8 + 8 * m) + jl;
           int64_t rr = rsub;
-          if (j < j1) {
-            rr = resolve_row(a, b, P, kv_base, j);
-            if (rr < 0) {
+          if (key_of(tile, m) < j1) {
+            if (raw_cur[m] >= 0 && raw_cur[m] < a.pool_rows)
+              rr = raw_cur[m];
+            else
               bad = 1;
-              rr = rsub;
-            }
           }
           own[m] = (int)rr;
+          raw_cur[m] = raw_nxt[m];
         }
+        load_ids(t + 2, raw_nxt);
 #pragma unroll 1
         for (int blk = 0; blk < 9; ++blk) produce(blk, own);
       }
@@ -419,7 +426,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
               const uint64_t adesc =
                   tc::smem_desc(sRing + sa * Cfg::kSlotBytes + kk * 2048, Cfg::kSlotBytes, 1024, tc::kSwizzle128B);
               const uint64_t bdesc =
-                  tc::smem_desc(sP + (u & 1) * Cfg::kPBuf + (kk >> 2) * Cfg::kPRegion + (kk & 3) * 32, 16, 1024,
+                  tc::smem_desc(sP + (kk >> 2) * Cfg::kPRegion + (kk & 3) * 32, 16, 1024,
                                 tc::kSwizzle128B);
               tc::mma_bf16_ss(tmem + m * Cfg::kOStride, adesc, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
             }
@@ -459,7 +466,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     bool my_abort = false;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
-      const int64_t key = j0 + (int64_t)t * kKeysPerTile + j;
+      const int64_t key = j0 + (int64_t)tile_at(t) * kKeysPerTile + j;
       uint64_t vis = 0;
       if (key < j1 && resolve_row(a, b, P, kv_base, key) >= 0) {  // rows outside the pool are excluded
         for (int tl = 0; tl < ntok; ++tl)
@@ -530,11 +537,9 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         if (tid < 2 * NQ) l_half *= ctl.alpha[tid >> 1];
         rescale = (t > 0) && ctl.rflag[t & 1];
       }
-      // P^T(t) reuses the buffer PV(t-2) read; a rescale of O^T also needs
-      // PV(t-1) to be complete.
-      if (t >= 2 && !my_abort)
-        my_abort = !mbar_wait(&ctl.pv_done[t & 1], ((t >> 1) - 1) & 1, &ctl.abort, a.status);
-      if (rescale && !my_abort)
+      // P^T(t) overwrites what PV(t-1) reads, and a rescale of O^T needs
+      // PV(t-1) complete as well.
+      if (t >= 1 && !my_abort)
         my_abort = !mbar_wait(&ctl.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, &ctl.abort, a.status);
       my_abort = __any_sync(0xffffffffu, my_abort);
       tc::fence_after_sync();
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         tc::tmem_wait_st();
       }
       if (!my_abort) {
-        const uint32_t pb_t = pbase + (t & 1) * Cfg::kPBuf;
+        const uint32_t pb_t = pbase;
         const float4* mu4 = reinterpret_cast<const float4*>(&ctl.muse[c0]);
 #pragma unroll
         for (int k4 = 0; k4 < HC / 4; ++k4) {
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
       named_bar_sync(1, kSoftmaxThreads);
       if (tid < 2 * NQ && !my_abort) {
         const int col = tid >> 1;
-        const uint32_t row = sP + (t & 1) * Cfg::kPBuf + (tid & 1) * Cfg::kPRegion + col * 128;
+        const uint32_t row = sP + (tid & 1) * Cfg::kPRegion + col * 128;
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {

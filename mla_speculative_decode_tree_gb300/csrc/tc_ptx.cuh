@@ -170,11 +170,6 @@ __device__ __forceinline__ void load_2d(uint32_t dst, const void* tmap, int x, i
       : "memory");
 }
 
-// Pull `bytes` of global memory into L2 ahead of use (16-byte aligned, multiple of 16).
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Contiguous shared -> global copy (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void store_bulk(void* gdst, uint32_t src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(src), "r"(bytes)
