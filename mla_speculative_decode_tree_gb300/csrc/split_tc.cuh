@@ -35,7 +35,7 @@
 //              writes P = exp2(s - m) as bf16 into P^T.  Per thread and
 //              column it accumulates the bf16 P (normalises O) and the fp32
 //              rounding residual p - bf16(p) (completes LSE).  Epilogue: O^T
-//              scaled by 1/l into shared memory, bulk-stored as 2 KB rows.
+//              scaled by 1/l and stored from TMEM straight to global memory.
 //   warp 4CG   TMEM allocation and the single MMA-issuing thread.
 //   warps 4CG+1..  gather (at most one per ring slot), taking turns block by block: cp.async 16-byte
 //              copies (from several warps: a single warp cannot issue them
@@ -87,7 +87,6 @@ struct TcCfg {
   static constexpr int kProducerWarps = (15 - kSoftmaxWarps) < kStages ? (15 - kSoftmaxWarps) : kStages;
   static_assert(kProducerWarps >= 1 && kProducerWarps <= kStages, "gather warps must not outnumber ring slots");
   static constexpr int kThreads = 32 * (kProducerWarp + kProducerWarps);
-  static_assert(NQ * 2048 <= kOffCtl, "epilogue staging must fit below the control block");
 };
 
 template <int NQ>
@@ -634,28 +633,23 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     }
     named_bar_sync(1, kSoftmaxThreads);
     if (!(f & 2)) {
-      // Stage O rows (fp32, 2 KB each) over the now idle Q / P^T / ring space.
-      float* stage = reinterpret_cast<float*>(smem);
+      // O straight from TMEM to global memory: thread (quad, lane) holds
+      // latent column 128m + j of query rows c0..c0+HC, so each warp store
+      // writes 32 consecutive columns (128 bytes) of one row.  Rows with
+      // nothing visible are not written (their LSE is -inf).
+      float* ocol = a.part_o + ((int64_t)s_idx * a.rows_max + grow0) * kDLatent + j;
 #pragma unroll 1
       for (int m = 0; m < 4; ++m) {
+        float v[HC];
 #pragma unroll
-        for (int c = 0; c < HC / 8; ++c) {
-          float v[8];
-          tc::tmem_ld8(t_lane + m * Cfg::kOStride + c0 + 8 * c, v);
-          tc::tmem_wait_ld();
+        for (int c = 0; c < HC / 8; ++c) tc::tmem_ld8(t_lane + m * Cfg::kOStride + c0 + 8 * c, &v[8 * c]);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int n = c0 + 8 * c + k;
-            stage[n * kDLatent + 128 * m + j] = v[k] * ctl.alpha[n];
-          }
+        for (int k = 0; k < HC; ++k) {
+          const int n = c0 + k;
+          const float inv_l = ctl.alpha[n];
+          if (n < nrows && inv_l > 0.f) ocol[(int64_t)n * kDLatent + 128 * m] = v[k] * inv_l;
         }
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, kSoftmaxThreads);
-      if (tid < nrows && ctl.alpha[tid] > 0.f) {
-        tma::store_bulk(a.part_o + ((int64_t)s_idx * a.rows_max + grow0 + tid) * kDLatent, sbase + tid * 2048, 2048);
-        tma::store_commit();
-        tma::store_wait_read();
       }
     }
     tc::fence_before_sync();

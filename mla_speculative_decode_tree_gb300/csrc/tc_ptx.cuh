@@ -70,16 +70,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Arrive once on the barrier at the same shared-memory offset in every CTA of
-// ctaMask (this cluster) when this thread's previously issued MMAs complete.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          static_cast<uint32_t>(__cvta_generic_to_shared(bar))),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // ---- TMEM <-> registers, 32 lanes x 32 bits, 16 consecutive columns ---------
 // Warp w may only touch lanes [32*(w%4), 32*(w%4)+32); thread t gets lane 32*(w%4)+t.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -137,30 +127,6 @@ __device__ __forceinline__ void arrive_expect_tx(uint64_t* bar, uint32_t bytes) 
                : "memory");
 }
 
-// Four rows y0..y3 of a 2-D tensor, columns [x, x + box width), into four
-// consecutive box rows at dst (swizzled by shared-memory address).
-__device__ __forceinline__ void gather4(uint32_t dst, const void* tmap, int x, int y0, int y1, int y2, int y3,
-                                        uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-      "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
-      : "memory");
-}
-
-// gather4 written to the same shared-memory offset of every CTA in ctaMask;
-// each destination CTA's barrier at `bar`'s offset receives the bytes.
-__device__ __forceinline__ void gather4_multicast(uint32_t dst, const void* tmap, int x, int y0, int y1, int y2, int y3,
-                                                  uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-      "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "h"(cta_mask)
-      : "memory");
-}
-
 // One box of a 2-D tensor at (x, y); rows past the tensor end read as zeros.
 __device__ __forceinline__ void load_2d(uint32_t dst, const void* tmap, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -170,27 +136,6 @@ __device__ __forceinline__ void load_2d(uint32_t dst, const void* tmap, int x, i
       : "memory");
 }
 
-// Contiguous shared -> global copy (16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void store_bulk(void* gdst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(src), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until the shared-memory sources of this thread's bulk stores have been read.
-__device__ __forceinline__ void store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
 }  // namespace tma
 
-// ---- thread-block clusters --------------------------------------------------
-namespace cluster {
-__device__ __forceinline__ uint32_t ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA in the cluster; release/acquire ordering.
-__device__ __forceinline__ void sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-}  // namespace cluster
 }  // namespace mlav
