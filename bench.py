@@ -452,9 +452,20 @@ def cpu_baseline(wl, budget_s=15.0, rows=None):
     t0 = time.perf_counter()
     ref.verify(wl, rows=rows, nthreads=cores)
     dt = time.perf_counter() - t0
-    us_call = dt / rows.size * n_all * 1e6
-    return {"value": round(us_call, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "%d of %d output rows (token x head) of the workload, fp64, %.1f s wall" % (rows.size, n_all, dt)}
+    reps = 1
+    if rows.size == n_all and dt < 0.5 * budget_s:
+        # a whole call is cheap: repeat it to fill the budget
+        more = int(min(1000, budget_s / max(dt, 1e-6))) - 1
+        for _ in range(more):
+            ref.verify(wl, rows=rows, nthreads=cores)
+        reps += more
+        dt = time.perf_counter() - t0
+    us_call = dt / reps / rows.size * n_all * 1e6
+    if reps > 1:
+        sample = "%d whole calls (all %d output rows each), fp64, %.1f s wall" % (reps, n_all, dt)
+    else:
+        sample = "%d of %d output rows (token x head) of the workload, fp64, %.1f s wall" % (rows.size, n_all, dt)
+    return {"value": round(us_call, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
 
 
 def run_reference(args):
@@ -491,6 +502,44 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def record_traffic(csv_path: str, workload: str) -> dict:
+    """Store the split kernel's DRAM bytes per launch from an ncu CSV capture
+    (metrics dram__bytes_read.sum and dram__bytes_write.sum) under the current
+    kernel source hash, for the `traffic` field of later runs."""
+    import csv
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+    per_launch = {}
+    with open(csv_path) as f:
+        rows = csv.DictReader(line for line in f if line.startswith('"'))
+        for r in rows:
+            if "split_tc_kernel" not in r.get("Kernel Name", "") and "split_simt_kernel" not in r.get("Kernel Name", ""):
+                continue
+            name = r.get("Metric Name", "")
+            if name not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                continue
+            v = float(r["Metric Value"].replace(",", "")) * scale.get(r.get("Metric Unit", "byte"), 1)
+            per_launch.setdefault(r["ID"], {})[name] = v
+    launches = [d for d in per_launch.values() if len(d) == 2]
+    if not launches:
+        raise SystemExit("no split-kernel launch with both DRAM metrics in %s" % csv_path)
+    bytes_avg = sum(d["dram__bytes_read.sum"] + d["dram__bytes_write.sum"] for d in launches) / len(launches)
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        rec = {}
+    rec[workload] = {"source_hash": kernel_source_hash(), "dram_bytes_per_launch": int(round(bytes_avg)),
+                     "launches": len(launches),
+                     "read_bytes": int(round(sum(d["dram__bytes_read.sum"] for d in launches) / len(launches))),
+                     "write_bytes": int(round(sum(d["dram__bytes_write.sum"] for d in launches) / len(launches)))}
+    os.makedirs(os.path.dirname(path), exist_ok=True)
+    with open(path, "w") as f:
+        json.dump(rec, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return rec[workload]
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -501,7 +550,12 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="store the split kernel's DRAM bytes per launch from an ncu CSV for --workload, then exit")
     args = ap.parse_args(argv)
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.workload)))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
