@@ -235,11 +235,35 @@ def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False):
     t_split = time_graph(torch, g_split.replay, steps, warmup, flush, stream)
     status = v.status(stream)
     alg = algorithmic(wl)
-    res = dict(wl=wl, info=info, t_call=t_call, t_split=t_split, alg=alg, status=status)
+    res = dict(wl=wl, info=info, t_call=t_call, t_split=t_split, alg=alg, status=status,
+               tree_mask=measure_tree_mask(torch, wl, v.plan, stream, steps, warmup, flush))
     if with_e2e:
         res["e2e"] = measure_e2e(torch, wl, v, stream, steps, warmup, flush)
     del g_call, g_split, d
     return res
+
+
+def measure_tree_mask(torch, wl, plan, stream, steps, warmup, flush):
+    """Device tree-mask build (parents -> packed mask) timed alone, graph-replayed,
+    L2 flushed before each launch; checked bit for bit against the call's mask."""
+    from mla_speculative_decode_tree_gb300 import binding as B
+
+    dev = B.device_inputs(wl)
+    parents = torch.from_numpy(np.concatenate([np.asarray(p, np.int32) for p in wl["parents"]])).cuda()
+    mask = torch.zeros_like(dev["custom_mask"])
+    mip = torch.zeros_like(dev["mask_indptr"])
+
+    def build():
+        B.mla_verify_build_tree_mask(plan, parents, dev["kv_indptr"], wl["B"], mask, mip, stream=stream)
+
+    g = capture(torch, build, stream)
+    t = time_graph(torch, g.replay, steps, warmup, flush, stream)
+    torch.cuda.synchronize()
+    n = (wl["T"] * int(sum(int(p) + wl["T"] for p in wl["prefix_lens"])) + 7) // 8
+    same = bool(torch.equal(mask[:n], dev["custom_mask"][:n]) and torch.equal(mip, dev["mask_indptr"]))
+    del g
+    return {"us": round(statistics.mean(t) * 1e3, 3), "mask_bytes": n, "matches_input_mask": same,
+            "launches_per_call": 1}
 
 
 def measure_e2e(torch, wl, v, stream, steps, warmup, flush):
@@ -291,7 +315,7 @@ def summarize(res, peaks):
         tflops=alg["flops"] / (t_call_us * 1e-6) / 1e12,
         roofline_frac=max(t_hbm, t_mma) / t_call_us, bound="tensor" if t_mma >= t_hbm else "hbm",
         kernel="tcgen05" if res["info"].kernel == 1 else "cuda-core", rows_per_cta=res["info"].rows_per_cta,
-        status=res["status"])
+        status=res["status"], tree_mask=res.get("tree_mask"))
 
 
 def run_gpu(args):
@@ -375,6 +399,7 @@ def run_gpu(args):
     t_split = time_graph(torch, g_split.replay, args.steps, 3, flush, stream)
     status = v.status(stream)
     e2e = measure_e2e(torch, wl, v, stream, args.steps, args.warmup, flush)
+    tree_mask = measure_tree_mask(torch, wl, v.plan, stream, min(args.steps, 50), 3, flush)
     clocks = sampler.stop()
 
     alg = algorithmic(wl)
@@ -408,6 +433,7 @@ def run_gpu(args):
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": 2 * args.steps,
+        "tree_mask_build": tree_mask,
         "clocks": clocks,
         "device_status": status,
         "gpu": phys.name,

@@ -180,6 +180,37 @@ int mla_verify_read_status(mla_verify_plan_t plan, void* workspace, void* stream
                            uint32_t* device_status);
 
 /*
+ * Build the packed visibility mask of a verify call on the device from the
+ * draft trees' parent arrays (one kernel on `stream`; no allocation, no host
+ * synchronisation, so it can be captured in the same CUDA graph as
+ * mla_verify_run).  The pages build the tree and the mask on the host every
+ * step and measured that cost [Capture Safety to MoE Ceiling, §"Phase 2e:
+ * The Occupancy Epiphany and the 3-6x Speedup"]; the layout written is the
+ * one mla_verify_run reads [Custom sm_120 Verify Kernel, §"The Debugging
+ * Gauntlet"].
+ *
+ *  parents      int32 [batch*q_len]: parents[b*q_len + i] is the parent node of
+ *               draft token i of request b, -1 for a root; a parent precedes its
+ *               child (-1 <= parent < i).  A link outside that range ends the
+ *               ancestor walk (the token then sees only the nodes walked).
+ *  kv_indptr    int32 [batch+1], non-decreasing: P_b = kv_indptr[b+1] - kv_indptr[b]
+ *  batch        0 <= batch <= max_batch (0 enqueues nothing)
+ *  custom_mask  uint8 output: bit mask_indptr[b] + i*(P_b+q_len) + j (LSB-first) is 1
+ *               when j < P_b, or when draft node j - P_b is i or an ancestor of i
+ *  mask_bytes   capacity of custom_mask; bits past it are not written
+ *  mask_indptr  int32 [batch] output: q_len * sum_{b'<b} (P_b' + q_len)
+ *  stream       cudaStream_t (NULL = legacy default stream)
+ *
+ * Bits past the last request's block, within the last byte, are written 0.
+ * The plan supplies q_len and the grid (sized for max_batch requests of
+ * max_kv_len keys).  Errors: EINVAL (NULL or misaligned pointer, batch outside
+ * [0, max_batch]), ECUDA.
+ */
+int mla_verify_build_tree_mask(mla_verify_plan_t plan, const int32_t* parents, const int32_t* kv_indptr,
+                               int32_t batch, uint8_t* custom_mask, size_t mask_bytes,
+                               int32_t* mask_indptr, void* stream);
+
+/*
  * mla_verify_run without a workspace argument, for callers that have no way
  * to obtain device memory of their own: for example a plugin host that hands
  * a kernel only its input and output buffers, or a latency-critical path that

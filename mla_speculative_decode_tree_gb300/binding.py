@@ -26,7 +26,7 @@ MLA_VERIFY_FORCE_SIMT = 0x1
 
 EXPORTED = ("mla_verify_plan", "mla_verify_plan_describe", "mla_verify_run", "mla_verify_split",
             "mla_verify_merge", "mla_verify_workspace_init", "mla_verify_read_status", "mla_verify_destroy",
-            "mla_verify_strerror", "mla_verify_run_noalloc")
+            "mla_verify_strerror", "mla_verify_run_noalloc", "mla_verify_build_tree_mask")
 
 
 class MlaVerifyParams(ctypes.Structure):
@@ -69,6 +69,7 @@ def load(path: str = LIB_PATH):
     lib.mla_verify_merge.argtypes = [P, i32, i32, P, sz, P, P, P]
     lib.mla_verify_run_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, i32, f32, i32, P, P, P]
     lib.mla_verify_workspace_init.argtypes = [P, P, sz, P]
+    lib.mla_verify_build_tree_mask.argtypes = [P, P, P, i32, P, sz, P, P]
     lib.mla_verify_read_status.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_verify_destroy.argtypes = [P]
     lib.mla_verify_strerror.argtypes = [ctypes.c_int]
@@ -187,6 +188,15 @@ def mla_verify_merge(plan: Plan, batch: int, nsplit: int, workspace, o, lse, str
     rc = load().mla_verify_merge(ctypes.c_void_p(plan.handle), int(batch), int(nsplit), _ptr(workspace),
                                  int(ws_bytes), _ptr(o), _ptr(lse), _stream(stream))
     _check(rc, "mla_verify_merge")
+
+
+def mla_verify_build_tree_mask(plan: Plan, parents, kv_indptr, batch: int, custom_mask, mask_indptr, stream=None,
+                               mask_bytes: Optional[int] = None):
+    """Device tree-mask build: parents int32 [batch*q_len] -> packed custom_mask, mask_indptr int32 [batch]."""
+    nbytes = custom_mask.numel() * custom_mask.element_size() if mask_bytes is None else mask_bytes
+    rc = load().mla_verify_build_tree_mask(ctypes.c_void_p(plan.handle), _ptr(parents), _ptr(kv_indptr), int(batch),
+                                           _ptr(custom_mask), int(nbytes), _ptr(mask_indptr), _stream(stream))
+    _check(rc, "mla_verify_build_tree_mask")
 
 
 def mla_verify_workspace_init(plan: Plan, workspace, stream=None):

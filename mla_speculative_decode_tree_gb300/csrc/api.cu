@@ -301,6 +301,22 @@ int mla_verify_run(mla_verify_plan_t pl, const void* q_nope_absorbed, const void
   return mla_verify_merge(pl, batch, nsplit, workspace, workspace_bytes, o, lse, stream);
 }
 
+int mla_verify_build_tree_mask(mla_verify_plan_t pl, const int32_t* parents, const int32_t* kv_indptr,
+                               int32_t batch, uint8_t* custom_mask, size_t mask_bytes, int32_t* mask_indptr,
+                               void* stream) {
+  if (!pl || batch < 0 || batch > pl->p.max_batch) return MLA_VERIFY_EINVAL;
+  if (batch == 0) return MLA_VERIFY_OK;
+  if (!parents || !kv_indptr || !custom_mask || !mask_indptr || !aligned(parents, 4) || !aligned(kv_indptr, 4) ||
+      !aligned(mask_indptr, 4))
+    return MLA_VERIFY_EINVAL;
+  int rc;
+  if ((rc = check_device()) != MLA_VERIFY_OK) return rc;
+  const int64_t max_bytes = ((int64_t)pl->p.max_batch * pl->p.q_len * pl->p.max_kv_len + 7) / 8;
+  cudaError_t e = launch_tree_mask(parents, kv_indptr, batch, pl->p.q_len, custom_mask, (int64_t)mask_bytes,
+                                   mask_indptr, max_bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
+}
+
 int mla_verify_workspace_init(mla_verify_plan_t pl, void* workspace, size_t workspace_bytes, void* stream) {
   if (!pl || !workspace || workspace_bytes < pl->ws_bytes || !aligned(workspace, 256)) return MLA_VERIFY_EINVAL;
   cudaError_t e = cudaMemsetAsync(workspace, 0, kWsHeader, static_cast<cudaStream_t>(stream));

@@ -181,6 +181,8 @@ MLAV_DECLARE_TC(80)
 MLAV_DECLARE_TC(96)
 #undef MLAV_DECLARE_TC
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* kv_indptr, int batch, int T, uint8_t* mask,
+                             int64_t mask_bytes, int32_t* mask_indptr, int64_t max_bytes, cudaStream_t stream);
 int merge_blocks(int rows);
 
 constexpr int kSimtRowsPerCta = 8;  // one warp per query row
