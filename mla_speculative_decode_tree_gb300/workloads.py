@@ -101,20 +101,23 @@ def pack_bits_lsb(bits: np.ndarray) -> np.ndarray:
     return np.packbits(np.asarray(bits, dtype=np.uint8).reshape(-1), bitorder="little")
 
 
-def build_mask(prefix_lens: Sequence[int], parents: Sequence[np.ndarray], T: int,
+def build_mask(prefix_lens: Sequence[int], parents: Sequence[np.ndarray], T,
                prefix_visible: Optional[List[np.ndarray]] = None):
     """Dense per-request visibility rows -> (packed bytes, bit offsets, dense list).
 
-    Request b contributes a row-major [T, P_b + T] block; the first P_b columns
-    are prefix tokens (visible unless ``prefix_visible`` says otherwise), the
-    last T columns follow the draft tree.
+    Request b contributes a row-major [T_b, P_b + T_b] block (T an int, or one
+    draft-token count per request); the first P_b columns are prefix tokens
+    (visible unless ``prefix_visible`` says otherwise), the last T_b columns
+    follow the draft tree.
     """
+    Ts = [int(t) for t in T] if hasattr(T, "__len__") else [int(T)] * len(prefix_lens)
     dense = []
     offsets = np.zeros(len(prefix_lens), dtype=np.int64)
     total = 0
     for b, P in enumerate(prefix_lens):
-        L = P + T
-        m = np.zeros((T, L), dtype=bool)
+        Tb = Ts[b]
+        L = P + Tb
+        m = np.zeros((Tb, L), dtype=bool)
         if prefix_visible is None:
             m[:, :P] = True
         else:
@@ -122,7 +125,7 @@ def build_mask(prefix_lens: Sequence[int], parents: Sequence[np.ndarray], T: int
         m[:, P:] = tree_visibility(parents[b])
         dense.append(m)
         offsets[b] = total
-        total += T * L
+        total += Tb * L
     flat = np.concatenate([d.reshape(-1) for d in dense]) if dense else np.zeros(0, bool)
     packed = pack_bits_lsb(flat)
     if packed.size == 0:
@@ -332,3 +335,48 @@ def tiny_workload(B: int, H: int, T: int, prefix_lens: Sequence[int], pool_rows:
     cfg = VerifyConfig("adhoc", B=B, H=H, T=T, prefix=0, pool_rows=pool_rows, nsplit=nsplit, tree=tree,
                        seed=seed)
     return make_workload(cfg, seed=seed, prefix_override=list(prefix_lens))
+
+
+def varlen_workload(B: int, H: int, T_list: Sequence[int], prefix_lens: Sequence[int], pool_rows: int,
+                    seed: int, nsplit: int = 2, tree: str = "random", layout: str = "scattered") -> dict:
+    """A verify call whose requests have their own draft-token counts T_b.
+
+    Token rows of request b are qo_indptr[b] .. qo_indptr[b+1]-1 (qo_indptr =
+    [0, cumsum(T_b)]); its draft rows are out_cache_loc[qo_indptr[b] + t] and
+    its mask block is [T_b, P_b + T_b].  The query buffers hold B * max(T_b)
+    token rows (the tail past qo_indptr[B] is padding a device kernel may
+    read but never uses); ``T`` is max(T_b), the plan's q_len.
+    """
+    rng = np.random.default_rng(seed)
+    Ts = np.asarray([int(t) for t in T_list], dtype=np.int64)
+    assert Ts.shape == (B,) and (Ts >= 0).all()
+    T = max(1, int(Ts.max()) if B else 1)
+    pool = normal_bf16(rng, (pool_rows, D_ROW))
+    q_nope = normal_bf16(rng, (B * T, H, D_LATENT))
+    q_rope = normal_bf16(rng, (B * T, H, D_ROPE))
+    P = np.asarray(prefix_lens, dtype=np.int64)
+    n_tok = int(Ts.sum())
+    n_rows = int(P.sum()) + n_tok
+    if n_rows > pool_rows:
+        raise ValueError("pool smaller than the rows one call addresses")
+    phys = place_rows(rng, layout, n_rows, pool_rows)
+    kv_indptr = np.zeros(B + 1, dtype=np.int64)
+    kv_indptr[1:] = np.cumsum(P)
+    qo_indptr = np.zeros(B + 1, dtype=np.int64)
+    qo_indptr[1:] = np.cumsum(Ts)
+    kv_indices = phys[: int(P.sum())].astype(np.int32)
+    out_cache_loc = np.zeros(B * T, dtype=np.int32)  # capacity B*T, padding rows name pool row 0
+    out_cache_loc[:n_tok] = phys[int(P.sum()):]
+    parents = [chain_tree(int(t)) if tree == "chain" else random_tree(rng, int(t)) for t in Ts]
+    custom_mask, mask_indptr, dense = build_mask(P.tolist(), parents, Ts.tolist())
+    cfg = VerifyConfig("varlen", B=B, H=H, T=T, prefix=0, pool_rows=pool_rows, nsplit=nsplit, tree=tree,
+                       layout=layout, seed=seed)
+    return dict(
+        cfg=cfg, seed=seed, layout=layout,
+        B=B, H=H, T=T, T_list=Ts, qo_indptr=qo_indptr.astype(np.int32), n_tokens=n_tok,
+        pool_rows=pool_rows, nsplit=nsplit, sm_scale=cfg.sm_scale,
+        prefix_lens=P, pool=pool, q_nope=q_nope, q_rope=q_rope,
+        kv_indptr=kv_indptr.astype(np.int32), kv_indices=kv_indices, out_cache_loc=out_cache_loc,
+        custom_mask=custom_mask, mask_indptr=mask_indptr.astype(np.int32),
+        parents=parents, dense_mask=dense,
+    )

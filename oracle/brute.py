@@ -36,24 +36,36 @@ def brute_verify(wl: dict, rows: Optional[Sequence[int]] = None):
     scale = float(wl["sm_scale"])
     pool = wl["pool"]
     qn, qr = wl["q_nope"], wl["q_rope"]
+    # request b's tokens: token rows q0[b] .. q0[b] + Tb[b] - 1
+    if wl.get("qo_indptr") is not None:
+        qo = [int(x) for x in wl["qo_indptr"]]
+        q0 = qo[:-1]
+        Tb = [qo[b + 1] - qo[b] for b in range(B)]
+    else:
+        q0 = [b * T for b in range(B)]
+        Tb = [T] * B
+    owner = {}
+    for b in range(B):
+        for i in range(Tb[b]):
+            owner[q0[b] + i] = (b, i)
     if rows is None:
-        rows = range(B * T * H)
+        rows = range(sum(Tb) * H)
     outs, lses = [], []
     for r in rows:
         r = int(r)
         h = r % H
-        b, i = divmod(r // H, T)
+        b, i = owner[r // H]
         P = int(wl["kv_indptr"][b + 1]) - int(wl["kv_indptr"][b])
         seen = _ancestors_and_self(wl["parents"][b], i)
-        q = [_bf16(x) for x in qn[b * T + i, h]] + [_bf16(x) for x in qr[b * T + i, h]]
+        q = [_bf16(x) for x in qn[q0[b] + i, h]] + [_bf16(x) for x in qr[q0[b] + i, h]]
         scores, vals = [], []
-        for j in range(P + T):
+        for j in range(P + Tb[b]):
             if j < P:
                 row = int(wl["kv_indices"][int(wl["kv_indptr"][b]) + j])
             else:
                 if (j - P) not in seen:
                     continue
-                row = int(wl["out_cache_loc"][b * T + (j - P)])
+                row = int(wl["out_cache_loc"][q0[b] + (j - P)])
             k = [_bf16(x) for x in pool[row]]
             scores.append(scale * math.fsum(qa * ka for qa, ka in zip(q, k)))
             vals.append(k[:512])

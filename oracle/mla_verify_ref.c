@@ -6,14 +6,17 @@
  * and its Python binding) never calls it and shares no code with it.
  *
  * What it computes (plain definition, fp64, no blocking or fusion):
- * for every request b, draft token i < T and head h, over the L_b = P_b + T
- * keys of that request,
+ * for every request b, draft token i < T_b and head h, over the
+ * L_b = P_b + T_b keys of that request, where request b's tokens are the
+ * token rows q0_b .. q0_b + T_b - 1 (q0_b = qo_indptr[b] and
+ * T_b = qo_indptr[b+1] - qo_indptr[b]; without qo_indptr every request has
+ * T tokens and q0_b = b*T),
  *
  *   visible(j)  = bit (mask_indptr[b] + i*L_b + j) of custom_mask (LSB-first)
  *                 [Custom sm_120 Verify Kernel, §"The Debugging Gauntlet":
  *                  mask row stride is prefix + q_len; mask_indptr has B entries]
  *   row(j)      = kv_indices[kv_indptr[b] + j]        if j <  P_b
- *               = out_cache_loc[b*T + (j - P_b)]      if j >= P_b
+ *               = out_cache_loc[q0_b + (j - P_b)]     if j >= P_b
  *                 [Capture Safety to MoE Ceiling, §"The Architecture of Capture
  *                  Safety": two-array row selection]
  *   s_j         = sm_scale * ( sum_{d<512} q_nope[d]*kv[row(j), d]
@@ -79,6 +82,7 @@ static int mask_bit(const uint8_t* mask, int64_t bit, int mutation) {
 
 typedef struct {
   int B, H, T;
+  const int32_t* qo_indptr; /* NULL: request b has T tokens starting at token row b*T */
   const uint16_t* q_nope;
   const uint16_t* q_rope;
   const uint16_t* kv_pool;
@@ -92,6 +96,31 @@ typedef struct {
   int mutation;
 } problem_t;
 
+static int64_t q_start(const problem_t* p, int b) {
+  return p->qo_indptr ? (int64_t)p->qo_indptr[b] : (int64_t)b * p->T;
+}
+
+static int64_t q_count(const problem_t* p, int b) {
+  return p->qo_indptr ? (int64_t)p->qo_indptr[b + 1] - p->qo_indptr[b] : (int64_t)p->T;
+}
+
+/* Request and token of token row `tok` (a row some request owns). */
+static void token_owner(const problem_t* p, int64_t tok, int* b, int* i) {
+  if (!p->qo_indptr) {
+    *b = (int)(tok / p->T);
+    *i = (int)(tok % p->T);
+    return;
+  }
+  int r = 0;
+  while (r + 1 < p->B && q_start(p, r + 1) <= tok) ++r;  /* requests with no tokens are passed */
+  *b = r;
+  *i = (int)(tok - q_start(p, r));
+}
+
+static int64_t n_token_rows(const problem_t* p) {
+  return p->qo_indptr ? (int64_t)p->qo_indptr[p->B] : (int64_t)p->B * p->T;
+}
+
 /* Row of the pool that key position j of request b refers to; -1 if invalid. */
 static int64_t key_row(const problem_t* p, int b, int64_t P, int64_t j) {
   int64_t r;
@@ -99,15 +128,15 @@ static int64_t key_row(const problem_t* p, int b, int64_t P, int64_t j) {
     r = p->kv_indices[p->kv_indptr[b] + j];
   } else {
     int64_t t = j - P;
-    if (p->mutation == MUT_DRAFT_REVERSED) t = p->T - 1 - t;
-    r = p->out_cache_loc[(int64_t)b * p->T + t];
+    if (p->mutation == MUT_DRAFT_REVERSED) t = q_count(p, b) - 1 - t;
+    r = p->out_cache_loc[q_start(p, b) + t];
   }
   if (r < 0 || r >= p->pool_rows) return -1;
   return r;
 }
 
 static int key_visible(const problem_t* p, int b, int i, int64_t P, int64_t j) {
-  int64_t L = P + p->T;
+  int64_t L = P + q_count(p, b);
   int64_t stride = (p->mutation == MUT_MASK_STRIDE_PREFIX) ? P : L;
   int bb = b;
   if (p->mutation == MUT_MASK_INDPTR_NEXT) bb = (b + 1 < p->B) ? b + 1 : b;
@@ -140,9 +169,9 @@ static const uint16_t* value_row(const problem_t* p, int64_t row) {
 static int attend_range(const problem_t* p, int b, int i, int h, int64_t j0, int64_t j1,
                         double* s_buf, double* o, double* lse) {
   int64_t P = p->kv_indptr[b + 1] - p->kv_indptr[b];
-  int64_t L = (p->mutation == MUT_PREFIX_ONLY) ? P : P + p->T;
+  int64_t L = (p->mutation == MUT_PREFIX_ONLY) ? P : P + q_count(p, b);
   if (j1 > L) j1 = L;
-  int64_t qrow = (int64_t)b * p->T + i;
+  int64_t qrow = q_start(p, b) + i;
   double m = -INFINITY;
   for (int64_t j = j0; j < j1; ++j) {
     s_buf[j - j0] = -INFINITY;
@@ -175,26 +204,27 @@ static int attend_range(const problem_t* p, int b, int i, int h, int64_t j0, int
 static int64_t max_len(const problem_t* p) {
   int64_t mx = 0;
   for (int b = 0; b < p->B; ++b) {
-    int64_t L = (int64_t)(p->kv_indptr[b + 1] - p->kv_indptr[b]) + p->T;
+    int64_t L = (int64_t)(p->kv_indptr[b + 1] - p->kv_indptr[b]) + q_count(p, b);
     if (L > mx) mx = L;
   }
   return mx;
 }
 
 /*
- * Direct evaluation.  rows_sel lists global output rows r = (b*T + i)*H + h
- * (NULL = all B*T*H rows in order).  o_out is [n_sel, 512], lse_out [n_sel].
- * Returns 0, or -1 if some referenced pool row is out of range.
+ * Direct evaluation.  rows_sel lists global output rows r = (q0_b + i)*H + h
+ * (NULL = all token rows x H in order).  o_out is [n_sel, 512], lse_out
+ * [n_sel].  qo_indptr may be NULL (uniform T).  Returns 0, or -1 if some
+ * referenced pool row is out of range.
  */
-int oracle_mla_verify(int B, int H, int T, const uint16_t* q_nope, const uint16_t* q_rope,
+int oracle_mla_verify(int B, int H, int T, const int32_t* qo_indptr, const uint16_t* q_nope, const uint16_t* q_rope,
                       const uint16_t* kv_pool, int64_t pool_rows, const int32_t* kv_indptr,
                       const int32_t* kv_indices, const int32_t* out_cache_loc,
                       const uint8_t* custom_mask, const int32_t* mask_indptr, double sm_scale,
                       const int64_t* rows_sel, int64_t n_sel, double* o_out, double* lse_out,
                       int nthreads, int mutation) {
-  problem_t p = {B, H, T, q_nope, q_rope, kv_pool, pool_rows, kv_indptr, kv_indices,
+  problem_t p = {B, H, T, qo_indptr, q_nope, q_rope, kv_pool, pool_rows, kv_indptr, kv_indices,
                  out_cache_loc, custom_mask, mask_indptr, sm_scale, mutation};
-  int64_t n = rows_sel ? n_sel : (int64_t)B * T * H;
+  int64_t n = rows_sel ? n_sel : n_token_rows(&p) * H;
   int64_t Lmax = max_len(&p);
   int err = 0;
 #ifdef _OPENMP
@@ -209,9 +239,9 @@ int oracle_mla_verify(int B, int H, int T, const uint16_t* q_nope, const uint16_
     for (int64_t k = 0; k < n; ++k) {
       int64_t r = rows_sel ? rows_sel[k] : k;
       int h = (int)(r % H);
-      int64_t bi = r / H;
-      int b = (int)(bi / T), i = (int)(bi % T);
-      int64_t L = (int64_t)(kv_indptr[b + 1] - kv_indptr[b]) + T;
+      int b, i;
+      token_owner(&p, r / H, &b, &i);
+      int64_t L = (int64_t)(kv_indptr[b + 1] - kv_indptr[b]) + q_count(&p, b);
       if (attend_range(&p, b, i, h, 0, L, s_buf, o_out + k * D_LATENT, lse_out + k) != 0) {
 #pragma omp atomic write
         err = -1;
@@ -231,7 +261,7 @@ int oracle_mla_verify(int B, int H, int T, const uint16_t* q_nope, const uint16_
  * O = sum_s w_s O_s / sum_s w_s, LSE = M + ln sum_s w_s.  Empty or fully
  * masked splits carry lse_s = -inf and weight 0.
  */
-int oracle_mla_verify_split_merge(int B, int H, int T, const uint16_t* q_nope,
+int oracle_mla_verify_split_merge(int B, int H, int T, const int32_t* qo_indptr, const uint16_t* q_nope,
                                   const uint16_t* q_rope, const uint16_t* kv_pool,
                                   int64_t pool_rows, const int32_t* kv_indptr,
                                   const int32_t* kv_indices, const int32_t* out_cache_loc,
@@ -239,9 +269,9 @@ int oracle_mla_verify_split_merge(int B, int H, int T, const uint16_t* q_nope,
                                   double sm_scale, int nsplit, int64_t granule, int64_t min_chunk,
                                   const int64_t* rows_sel, int64_t n_sel, double* o_out,
                                   double* lse_out, int nthreads) {
-  problem_t p = {B, H, T, q_nope, q_rope, kv_pool, pool_rows, kv_indptr, kv_indices,
+  problem_t p = {B, H, T, qo_indptr, q_nope, q_rope, kv_pool, pool_rows, kv_indptr, kv_indices,
                  out_cache_loc, custom_mask, mask_indptr, sm_scale, MUT_NONE};
-  int64_t n = rows_sel ? n_sel : (int64_t)B * T * H;
+  int64_t n = rows_sel ? n_sel : n_token_rows(&p) * H;
   int64_t Lmax = max_len(&p);
   int err = 0;
   if (nsplit < 1 || granule < 1) return -2;
@@ -259,9 +289,9 @@ int oracle_mla_verify_split_merge(int B, int H, int T, const uint16_t* q_nope,
     for (int64_t k = 0; k < n; ++k) {
       int64_t r = rows_sel ? rows_sel[k] : k;
       int h = (int)(r % H);
-      int64_t bi = r / H;
-      int b = (int)(bi / T), i = (int)(bi % T);
-      int64_t L = (int64_t)(kv_indptr[b + 1] - kv_indptr[b]) + T;
+      int b, i;
+      token_owner(&p, r / H, &b, &i);
+      int64_t L = (int64_t)(kv_indptr[b + 1] - kv_indptr[b]) + q_count(&p, b);
       int64_t per = (L + nsplit - 1) / nsplit;
       int64_t chunk = ((per + granule - 1) / granule) * granule;
       if (chunk < min_chunk) chunk = min_chunk;

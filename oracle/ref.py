@@ -41,10 +41,10 @@ def _load():
             lib = ctypes.CDLL(_LIB)
             P = ctypes.c_void_p
             i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
-            lib.oracle_mla_verify.argtypes = [i32, i32, i32, P, P, P, i64, P, P, P, P, P, f64,
+            lib.oracle_mla_verify.argtypes = [i32, i32, i32, P, P, P, P, i64, P, P, P, P, P, f64,
                                               P, i64, P, P, i32, i32]
             lib.oracle_mla_verify.restype = i32
-            lib.oracle_mla_verify_split_merge.argtypes = [i32, i32, i32, P, P, P, i64, P, P, P, P, P,
+            lib.oracle_mla_verify_split_merge.argtypes = [i32, i32, i32, P, P, P, P, i64, P, P, P, P, P,
                                                           f64, i32, i64, i64, P, i64, P, P, i32]
             lib.oracle_mla_verify_split_merge.restype = i32
             lib.oracle_max_threads.argtypes = []
@@ -77,8 +77,22 @@ def _common(wl):
     return keep, ptrs
 
 
+def _qo(wl):
+    """qo_indptr (request token offsets) of a varlen call, else None (uniform T)."""
+    qo = wl.get("qo_indptr")
+    if qo is None:
+        return None, None
+    a, p = _c(qo, np.int32)
+    return a, p
+
+
+def n_token_rows(wl) -> int:
+    qo = wl.get("qo_indptr")
+    return int(qo[-1]) if qo is not None else wl["B"] * wl["T"]
+
+
 def _rows(wl, rows):
-    n_all = wl["B"] * wl["T"] * wl["H"]
+    n_all = n_token_rows(wl) * wl["H"]
     if rows is None:
         return None, None, n_all
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
@@ -94,7 +108,8 @@ def verify(wl: dict, rows: Optional[Sequence[int]] = None, nthreads: int = 0, mu
     o = np.zeros((n, 512), dtype=np.float64)
     lse = np.zeros(n, dtype=np.float64)
     scale = wl["sm_scale"] if sm_scale is None else sm_scale
-    rc = lib.oracle_mla_verify(wl["B"], wl["H"], wl["T"], qn, qr, pool, wl["pool"].shape[0], indptr, idx,
+    qo_keep, qo = _qo(wl)
+    rc = lib.oracle_mla_verify(wl["B"], wl["H"], wl["T"], qo, qn, qr, pool, wl["pool"].shape[0], indptr, idx,
                                ocl, mask, mindptr, float(scale), rp, n,
                                o.ctypes.data_as(ctypes.c_void_p), lse.ctypes.data_as(ctypes.c_void_p),
                                int(nthreads), int(mutation))
@@ -112,7 +127,8 @@ def verify_split_merge(wl: dict, nsplit: int, granule: int = 1, min_chunk: int =
     r, rp, n = _rows(wl, rows)
     o = np.zeros((n, 512), dtype=np.float64)
     lse = np.zeros(n, dtype=np.float64)
-    rc = lib.oracle_mla_verify_split_merge(wl["B"], wl["H"], wl["T"], qn, qr, pool, wl["pool"].shape[0],
+    qo_keep, qo = _qo(wl)
+    rc = lib.oracle_mla_verify_split_merge(wl["B"], wl["H"], wl["T"], qo, qn, qr, pool, wl["pool"].shape[0],
                                            indptr, idx, ocl, mask, mindptr, float(wl["sm_scale"]),
                                            int(nsplit), int(granule), int(min_chunk), rp, n,
                                            o.ctypes.data_as(ctypes.c_void_p),
