@@ -59,15 +59,16 @@ def workload_desc(cfg) -> str:
 
 def algorithmic(wl):
     """Algorithmic bytes and FLOPs of one verify call (and of its split kernel)."""
-    T, H = wl["T"], wl["H"]
+    H = wl["H"]
     P = np.asarray(wl["prefix_lens"], dtype=np.int64)
-    Lb = P + T
+    Tb = np.asarray(wl["T_list"], dtype=np.int64) if wl.get("T_list") is not None else np.full(len(P), wl["T"])
+    Lb = P + Tb
     N = int(Lb.sum())
-    R = int(len(P) * T * H)
-    mask_bytes = int((T * Lb).sum() // 8)
-    split_bytes = N * 1152 + 4 * int(P.sum()) + 4 * len(P) * T + mask_bytes + R * 1152
+    R = int(Tb.sum() * H)
+    mask_bytes = int((Tb * Lb).sum() // 8)
+    split_bytes = N * 1152 + 4 * int(P.sum()) + 4 * int(Tb.sum()) + mask_bytes + R * 1152
     call_bytes = split_bytes + R * 1028
-    flops = 2 * int((T * H * Lb).sum()) * (576 + 512)
+    flops = 2 * int((Tb * H * Lb).sum()) * (576 + 512)
     return dict(rows=N, kv_bytes=N * 1152, split_bytes=split_bytes, call_bytes=call_bytes, flops=flops)
 
 
@@ -220,9 +221,7 @@ def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False):
     scale = wl["sm_scale"]
 
     def call():
-        B.mla_verify_run(v.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
-                         d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], wl["B"], scale, v.plan.nsplit,
-                         v.workspace, v.o, v.lse, stream=stream)
+        v.run(d, wl["B"], scale, stream=stream)  # the varlen entry point when the workload has qo_indptr
 
     def split_only():
         B.mla_verify_split(v.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
@@ -230,13 +229,18 @@ def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False):
                            v.workspace, stream=stream)
 
     g_call = capture(torch, call, stream)
-    g_split = capture(torch, split_only, stream)
     t_call = time_graph(torch, g_call.replay, steps, warmup, flush, stream)
-    t_split = time_graph(torch, g_split.replay, steps, warmup, flush, stream)
+    if "qo_indptr" in d:  # no split-only entry point for varlen calls: report the whole call
+        g_split, t_split = None, t_call
+    else:
+        g_split = capture(torch, split_only, stream)
+        t_split = time_graph(torch, g_split.replay, steps, warmup, flush, stream)
     status = v.status(stream)
     alg = algorithmic(wl)
     res = dict(wl=wl, info=info, t_call=t_call, t_split=t_split, alg=alg, status=status,
-               tree_mask=measure_tree_mask(torch, wl, v.plan, stream, steps, warmup, flush))
+               # the device tree-mask builder serves uniform q_len calls
+               tree_mask=None if "qo_indptr" in d else measure_tree_mask(torch, wl, v.plan, stream, steps, warmup,
+                                                                         flush))
     if with_e2e:
         res["e2e"] = measure_e2e(torch, wl, v, stream, steps, warmup, flush)
     del g_call, g_split, d
@@ -440,7 +444,7 @@ def run_gpu(args):
     }
     if rank == 0 and not args.no_sweep:
         sweep = {}
-        for name in ("mid64k", "long185k_h8", "batch16_ragged"):
+        for name in ("mid64k", "long185k_h8", "batch16_ragged", "decode_b16", "varlen_b16"):
             try:
                 res = measure_workload(torch, name, min(args.steps, 30), 3, flush, stream)
                 s = summarize(res, peaks)

@@ -152,6 +152,32 @@ int mla_verify_run(mla_verify_plan_t plan, const void* q_nope_absorbed, const vo
                    void* workspace, size_t workspace_bytes, void* o, float* lse, void* stream);
 
 /*
+ * mla_verify_run for requests with their own numbers of draft tokens,
+ * T_b = qo_indptr[b+1] - qo_indptr[b] with 0 <= T_b <= the plan's q_len
+ * (T_b = 1 everywhere is plain decode on the same kernels).  Request b owns
+ * token rows qo_indptr[b] .. qo_indptr[b+1]-1 of q_nope_absorbed, q_rope, o
+ * and lse (output row (qo_indptr[b] + i)*num_heads + h); its draft rows are
+ * out_cache_loc[qo_indptr[b] + t]; its mask block is [T_b, P_b + T_b]
+ * row-major at bit mask_indptr[b] -- the layout of mla_verify_run with T
+ * replaced by T_b [Custom sm_120 Verify Kernel, §"The Debugging Gauntlet",
+ * bugs 2 and 3].
+ *
+ *  qo_indptr  int32 [batch+1], qo_indptr[0] = 0, non-decreasing
+ *  q_nope_absorbed, q_rope, o, lse: allocated for batch*q_len token rows (the
+ *             fixed-size buffers a captured call uses); rows from
+ *             qo_indptr[batch] on may be read but are never written
+ *  everything else as mla_verify_run.
+ *
+ * Errors as mla_verify_run, plus EINVAL for a NULL or misaligned qo_indptr.
+ */
+int mla_verify_run_varlen(mla_verify_plan_t plan, const void* q_nope_absorbed, const void* q_rope,
+                          const void* kv_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
+                          const int32_t* qo_indptr, const int32_t* out_cache_loc,
+                          const uint8_t* custom_mask, const int32_t* mask_indptr, int32_t batch,
+                          float sm_scale, int32_t nsplit, void* workspace, size_t workspace_bytes,
+                          void* o, float* lse, void* stream);
+
+/*
  * The two launches of mla_verify_run, separately: the split kernel (writes
  * the partials into the workspace) and the merge kernel (reads them, writes
  * o and lse).  Same arguments and errors as mla_verify_run; merge ignores

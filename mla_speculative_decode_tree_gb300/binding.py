@@ -26,7 +26,8 @@ MLA_VERIFY_FORCE_SIMT = 0x1
 
 EXPORTED = ("mla_verify_plan", "mla_verify_plan_describe", "mla_verify_run", "mla_verify_split",
             "mla_verify_merge", "mla_verify_workspace_init", "mla_verify_read_status", "mla_verify_destroy",
-            "mla_verify_strerror", "mla_verify_run_noalloc", "mla_verify_build_tree_mask")
+            "mla_verify_strerror", "mla_verify_run_noalloc", "mla_verify_build_tree_mask",
+            "mla_verify_run_varlen")
 
 
 class MlaVerifyParams(ctypes.Structure):
@@ -66,6 +67,7 @@ def load(path: str = LIB_PATH):
     run_args = [P, P, P, P, P, P, P, P, P, i32, f32, i32, P, sz]
     lib.mla_verify_run.argtypes = run_args + [P, P, P]
     lib.mla_verify_split.argtypes = run_args + [P]
+    lib.mla_verify_run_varlen.argtypes = run_args[:6] + [P] + run_args[6:] + [P, P, P]
     lib.mla_verify_merge.argtypes = [P, i32, i32, P, sz, P, P, P]
     lib.mla_verify_run_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, i32, f32, i32, P, P, P]
     lib.mla_verify_workspace_init.argtypes = [P, P, sz, P]
@@ -148,6 +150,18 @@ def mla_verify_plan_describe(plan: Plan) -> MlaVerifyPlanInfo:
     _check(load().mla_verify_plan_describe(ctypes.c_void_p(plan.handle), ctypes.byref(info)),
            "mla_verify_plan_describe")
     return info
+
+
+def mla_verify_run_varlen(plan: Plan, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, qo_indptr,
+                          out_cache_loc, custom_mask, mask_indptr, batch: int, sm_scale: float, nsplit: int,
+                          workspace, o, lse, stream=None, workspace_bytes: Optional[int] = None):
+    ws_bytes = plan.workspace_bytes if workspace_bytes is None else workspace_bytes
+    rc = load().mla_verify_run_varlen(ctypes.c_void_p(plan.handle), _ptr(q_nope_absorbed), _ptr(q_rope),
+                                      _ptr(kv_pool), _ptr(kv_indptr), _ptr(kv_indices), _ptr(qo_indptr),
+                                      _ptr(out_cache_loc), _ptr(custom_mask), _ptr(mask_indptr), int(batch),
+                                      float(sm_scale), int(nsplit), _ptr(workspace), int(ws_bytes), _ptr(o),
+                                      _ptr(lse), _stream(stream))
+    _check(rc, "mla_verify_run_varlen")
 
 
 def mla_verify_run(plan: Plan, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, out_cache_loc,
@@ -237,6 +251,8 @@ def device_inputs(wl: dict, device="cuda"):
         out_cache_loc=t(wl["out_cache_loc"].astype(np.int32), torch.int32),
         custom_mask=t(wl["custom_mask"].astype(np.uint8), torch.uint8),
         mask_indptr=t(wl["mask_indptr"].astype(np.int32), torch.int32),
+        **({"qo_indptr": t(wl["qo_indptr"].astype(np.int32), torch.int32)} if wl.get("qo_indptr") is not None
+           else {}),
     )
 
 
@@ -254,9 +270,17 @@ class Verifier:
         self.rows_max = rows
 
     def run(self, d: dict, batch: int, sm_scale: float, stream=None):
-        mla_verify_run(self.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
-                       d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], batch, sm_scale, self.plan.nsplit,
-                       self.workspace, self.o, self.lse, stream=stream)
+        """One call; with d["qo_indptr"] present, the varlen entry point.  Returns the
+        output buffers' first batch*q_len token rows (varlen: the call's rows come first)."""
+        if "qo_indptr" in d:
+            mla_verify_run_varlen(self.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"],
+                                  d["kv_indices"], d["qo_indptr"], d["out_cache_loc"], d["custom_mask"],
+                                  d["mask_indptr"], batch, sm_scale, self.plan.nsplit, self.workspace, self.o,
+                                  self.lse, stream=stream)
+        else:
+            mla_verify_run(self.plan, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
+                           d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], batch, sm_scale,
+                           self.plan.nsplit, self.workspace, self.o, self.lse, stream=stream)
         n = batch * self.plan.params.q_len
         return self.o[:n], self.lse[:n]
 
@@ -265,5 +289,5 @@ class Verifier:
 
 
 def verifier_for(wl: dict, flags: int = 0, nsplit: Optional[int] = None, device="cuda") -> Verifier:
-    L = int(max(wl["prefix_lens"])) + wl["T"] if len(wl["prefix_lens"]) else wl["T"]
+    L = int(max(wl["prefix_lens"])) + wl["T"] if len(wl["prefix_lens"]) else wl["T"]  # bounds P_b + T_b too
     return Verifier(wl["B"], wl["H"], wl["T"], L, wl["pool"].shape[0], nsplit or wl["nsplit"], flags, device)

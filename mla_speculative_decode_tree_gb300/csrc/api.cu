@@ -210,10 +210,14 @@ int mla_verify_plan_describe(mla_verify_plan_t pl, mla_verify_plan_info* info) {
   return MLA_VERIFY_OK;
 }
 
-int mla_verify_split(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_rope, const void* kv_pool,
-                     const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* out_cache_loc,
-                     const uint8_t* custom_mask, const int32_t* mask_indptr, int32_t batch, float sm_scale,
-                     int32_t nsplit, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_rope, const void* kv_pool,
+               const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* qo_indptr,
+               const int32_t* out_cache_loc, const uint8_t* custom_mask, const int32_t* mask_indptr, int32_t batch,
+               float sm_scale, int32_t nsplit, void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_common(pl, batch, nsplit, workspace, workspace_bytes);
   if (rc != MLA_VERIFY_OK || batch == 0) return rc;
   if (!q_nope_absorbed || !q_rope || !kv_pool || !kv_indptr || !out_cache_loc || !custom_mask || !mask_indptr)
@@ -235,6 +239,7 @@ int mla_verify_split(mla_verify_plan_t pl, const void* q_nope_absorbed, const vo
   a.out_cache_loc = out_cache_loc;
   a.mask = custom_mask;
   a.mask_indptr = mask_indptr;
+  a.qo_indptr = qo_indptr;
   a.batch = batch;
   a.H = pl->p.num_heads;
   a.T = pl->p.q_len;
@@ -268,8 +273,8 @@ int mla_verify_split(mla_verify_plan_t pl, const void* q_nope_absorbed, const vo
   return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
 }
 
-int mla_verify_merge(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, void* workspace, size_t workspace_bytes,
-                     void* o, float* lse, void* stream) {
+int merge_impl(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, const int32_t* qo_indptr, void* workspace,
+               size_t workspace_bytes, void* o, float* lse, void* stream) {
   int rc = check_common(pl, batch, nsplit, workspace, workspace_bytes);
   if (rc != MLA_VERIFY_OK || batch == 0) return rc;
   if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return MLA_VERIFY_EINVAL;
@@ -277,6 +282,9 @@ int mla_verify_merge(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, void* 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   MergeArgs m;
   m.rows = batch * pl->p.q_len * pl->p.num_heads;
+  m.qo_indptr = qo_indptr;
+  m.batch = batch;
+  m.H = pl->p.num_heads;
   m.nsplit = pl->p.nsplit;
   m.rows_max = pl->rows_max;
   m.part_lse = reinterpret_cast<const float*>(ws + pl->off_lse);
@@ -288,6 +296,23 @@ int mla_verify_merge(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, void* 
   return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
 }
 
+}  // namespace
+
+extern "C" {
+
+int mla_verify_split(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_rope, const void* kv_pool,
+                     const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* out_cache_loc,
+                     const uint8_t* custom_mask, const int32_t* mask_indptr, int32_t batch, float sm_scale,
+                     int32_t nsplit, void* workspace, size_t workspace_bytes, void* stream) {
+  return split_impl(pl, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, nullptr, out_cache_loc, custom_mask,
+                    mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, stream);
+}
+
+int mla_verify_merge(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, void* workspace, size_t workspace_bytes,
+                     void* o, float* lse, void* stream) {
+  return merge_impl(pl, batch, nsplit, nullptr, workspace, workspace_bytes, o, lse, stream);
+}
+
 int mla_verify_run(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_rope, const void* kv_pool,
                    const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* out_cache_loc,
                    const uint8_t* custom_mask, const int32_t* mask_indptr, int32_t batch, float sm_scale,
@@ -295,10 +320,25 @@ int mla_verify_run(mla_verify_plan_t pl, const void* q_nope_absorbed, const void
   int rc = check_common(pl, batch, nsplit, workspace, workspace_bytes);
   if (rc != MLA_VERIFY_OK || batch == 0) return rc;
   if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return MLA_VERIFY_EINVAL;
-  rc = mla_verify_split(pl, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, out_cache_loc, custom_mask,
-                        mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, stream);
+  rc = split_impl(pl, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, nullptr, out_cache_loc, custom_mask,
+                  mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, stream);
   if (rc != MLA_VERIFY_OK) return rc;
-  return mla_verify_merge(pl, batch, nsplit, workspace, workspace_bytes, o, lse, stream);
+  return merge_impl(pl, batch, nsplit, nullptr, workspace, workspace_bytes, o, lse, stream);
+}
+
+int mla_verify_run_varlen(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_rope,
+                          const void* kv_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
+                          const int32_t* qo_indptr, const int32_t* out_cache_loc, const uint8_t* custom_mask,
+                          const int32_t* mask_indptr, int32_t batch, float sm_scale, int32_t nsplit,
+                          void* workspace, size_t workspace_bytes, void* o, float* lse, void* stream) {
+  int rc = check_common(pl, batch, nsplit, workspace, workspace_bytes);
+  if (rc != MLA_VERIFY_OK || batch == 0) return rc;
+  if (!qo_indptr || !aligned(qo_indptr, 4)) return MLA_VERIFY_EINVAL;
+  if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return MLA_VERIFY_EINVAL;
+  rc = split_impl(pl, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, qo_indptr, out_cache_loc,
+                  custom_mask, mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, stream);
+  if (rc != MLA_VERIFY_OK) return rc;
+  return merge_impl(pl, batch, nsplit, qo_indptr, workspace, workspace_bytes, o, lse, stream);
 }
 
 int mla_verify_build_tree_mask(mla_verify_plan_t pl, const int32_t* parents, const int32_t* kv_indptr,

@@ -30,6 +30,8 @@ struct SplitArgs {
   const int32_t* out_cache_loc;  // [B*T]
   const uint8_t* mask;           // packed bits LSB-first
   const int32_t* mask_indptr;    // [B] bit offsets
+  const int32_t* qo_indptr;      // [B+1] first token row of each request, or null: request b owns
+                                 // token rows b*T .. b*T+T-1 (T = the plan's q_len, the maximum)
   int32_t batch, H, T, nsplit;
   int64_t pool_rows;
   int64_t rows_max;              // max_batch*T*H: row stride of one split's partials
@@ -46,7 +48,9 @@ struct TcMaps {  // CUtensorMap carries its own (64-byte or larger) alignment
 };
 
 struct MergeArgs {
-  int32_t rows;      // batch*T*H rows to produce
+  int32_t rows;      // batch*T*H rows (the most a call can have)
+  const int32_t* qo_indptr;  // null, or [batch+1]: only rows below qo_indptr[batch]*H exist
+  int32_t batch, H;
   int32_t nsplit;
   int64_t rows_max;
   const float* part_lse;
@@ -147,19 +151,34 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 // ---- index helpers --------------------------------------------------------
-// Pool row of key position j of request b (prefix from kv_indices, drafts
-// from out_cache_loc); -1 when it lies outside [0, pool_rows).
-__device__ __forceinline__ int64_t resolve_row(const SplitArgs& a, int b, int64_t P, int64_t kv_base,
+// Token rows of request b: the first one (q0) and how many (at most T).
+struct RequestTokens {
+  int64_t q0;
+  int n;
+};
+__device__ __forceinline__ RequestTokens request_tokens(const SplitArgs& a, int b) {
+  if (!a.qo_indptr) return {(int64_t)b * a.T, a.T};
+  const int64_t q0 = a.qo_indptr[b];
+  int64_t n = (int64_t)a.qo_indptr[b + 1] - q0;
+  n = n < 0 ? 0 : (n > a.T ? a.T : n);  // the contract bounds T_b by q_len
+  return {q0, (int)n};
+}
+
+// Pool row of key position j of a request (prefix from kv_indices, drafts
+// from out_cache_loc at the request's token rows q0..); -1 when it lies
+// outside [0, pool_rows).
+__device__ __forceinline__ int64_t resolve_row(const SplitArgs& a, int64_t q0, int64_t P, int64_t kv_base,
                                                int64_t j) {
   int64_t r = (j < P) ? (int64_t)__ldg(a.kv_indices + kv_base + j)
-                      : (int64_t)__ldg(a.out_cache_loc + (int64_t)b * a.T + (j - P));
+                      : (int64_t)__ldg(a.out_cache_loc + q0 + (j - P));
   return (r >= 0 && r < a.pool_rows) ? r : -1;
 }
 
 // The raw index entry of key position j (no range check): lets a caller issue
 // the load early and check it when the value is used.
-__device__ __forceinline__ int32_t load_row_id(const SplitArgs& a, int b, int64_t P, int64_t kv_base, int64_t j) {
-  return (j < P) ? __ldg(a.kv_indices + kv_base + j) : __ldg(a.out_cache_loc + (int64_t)b * a.T + (j - P));
+__device__ __forceinline__ int32_t load_row_id(const SplitArgs& a, int64_t q0, int64_t P, int64_t kv_base,
+                                               int64_t j) {
+  return (j < P) ? __ldg(a.kv_indices + kv_base + j) : __ldg(a.out_cache_loc + q0 + (j - P));
 }
 
 __device__ __forceinline__ uint32_t mask_bit(const uint8_t* mask, int64_t bit) {

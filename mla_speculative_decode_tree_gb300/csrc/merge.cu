@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(64 * kRowsPerBlock) merge_kernel(MergeArgs a) 
   const int row = blockIdx.x * kRowsPerBlock + (warp >> 1);
   const int half = warp & 1;
   if (row >= a.rows) return;
+  if (a.qo_indptr && (int64_t)row >= (int64_t)a.qo_indptr[a.batch] * a.H) return;  // past the call's tokens
 
   float M = -INFINITY;
   for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, a.part_lse[(int64_t)s * a.rows_max + row]);

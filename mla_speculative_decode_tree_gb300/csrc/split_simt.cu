@@ -33,15 +33,16 @@ __global__ void __launch_bounds__(32 * kSimtRowsPerCta) split_simt_kernel(SplitA
   const int s = blockIdx.y;
   const int64_t kv_base = a.kv_indptr[b];
   const int64_t P = (int64_t)a.kv_indptr[b + 1] - kv_base;
-  const int64_t L = P + a.T;
+  const RequestTokens rq = request_tokens(a, b);
+  const int64_t L = P + rq.n;
   const int64_t chunk = chunk_len(L, a.nsplit);
   const int64_t j0 = (int64_t)s * chunk;
   const int64_t j1 = (j0 + chunk < L) ? j0 + chunk : L;
-  const int rows_b = a.T * a.H;
+  const int rows_b = rq.n * a.H;
   const int r = blockIdx.x * kSimtRowsPerCta + warp;
   if (r >= rows_b) return;
   const int i = r / a.H;
-  const int64_t grow = (int64_t)b * rows_b + r;  // == (b*T + i)*H + h
+  const int64_t grow = rq.q0 * a.H + r;  // == (q0 + i)*H + h
   float* lse_out = a.part_lse + (int64_t)s * a.rows_max + grow;
   if (j0 >= j1) {
     if (lane == 0) *lse_out = -INFINITY;
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(32 * kSimtRowsPerCta) split_simt_kernel(SplitA
       vis[u] = (j < j1) && mask_bit(a.mask, mask_row + j);
       va[u] = vb[u] = vr[u] = make_uint4(0, 0, 0, 0);
       if (vis[u]) {
-        const int64_t row = resolve_row(a, b, P, kv_base, j);
+        const int64_t row = resolve_row(a, rq.q0, P, kv_base, j);
         if (row >= 0) {
           const uint4* kv = reinterpret_cast<const uint4*>(a.kv_pool + row * kDRow);
           va[u] = __ldg(kv + lane);

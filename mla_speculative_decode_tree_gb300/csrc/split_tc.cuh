@@ -179,15 +179,16 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
 
   const int64_t kv_base = a.kv_indptr[b];
   const int64_t P = (int64_t)a.kv_indptr[b + 1] - kv_base;
-  const int64_t L = P + a.T;
+  const RequestTokens rq = request_tokens(a, b);
+  const int64_t L = P + rq.n;
   const int64_t chunk = chunk_len(L, a.nsplit);
   const int64_t j0 = (int64_t)s_idx * chunk;
   const int64_t j1 = (j0 + chunk < L) ? j0 + chunk : L;
-  const int rows_b = a.T * a.H;
+  const int rows_b = rq.n * a.H;
   const int r0 = g * NQ;
   if (r0 >= rows_b) return;
   const int nrows = (rows_b - r0 < NQ) ? rows_b - r0 : NQ;
-  const int64_t grow0 = (int64_t)b * rows_b + r0;
+  const int64_t grow0 = rq.q0 * a.H + r0;  // global row of the group's first row
   float* lse_out = a.part_lse + (int64_t)s_idx * a.rows_max + grow0;
   if (j0 >= j1) {
     for (int n = tid; n < nrows; n += kTcThreads) lse_out[n] = -INFINITY;
@@ -285,10 +286,10 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int64_t j = key_of(tile, m);
-        raw[m] = (t < nt && j < j1) ? load_row_id(a, b, P, kv_base, j) : -1;
+        raw[m] = (t < nt && j < j1) ? load_row_id(a, rq.q0, P, kv_base, j) : -1;
       }
     };
-    int64_t rsub = resolve_row(a, b, P, kv_base, j0);
+    int64_t rsub = resolve_row(a, rq.q0, P, kv_base, j0);
     int raw_cur[4], raw_nxt[4];
     load_ids(0, raw_cur);
     load_ids(1, raw_nxt);
@@ -467,7 +468,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     for (int t = 0; t < nt; ++t) {
       const int64_t key = j0 + (int64_t)tile_at(t) * kKeysPerTile + j;
       uint64_t vis = 0;
-      if (key < j1 && resolve_row(a, b, P, kv_base, key) >= 0) {  // rows outside the pool are excluded
+      if (key < j1 && resolve_row(a, rq.q0, P, kv_base, key) >= 0) {  // rows outside the pool are excluded
         for (int tl = 0; tl < ntok; ++tl)
           if (mask_bit(a.mask, mask_base + (int64_t)tl * L + key)) vis |= ctl.colmask[tl][half];
       }

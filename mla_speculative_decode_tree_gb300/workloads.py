@@ -178,6 +178,7 @@ class VerifyConfig:
     layout: str = "scattered"  # "scattered" | "sorted"
     needle: bool = False
     seed: int = 0
+    T_range: Optional[tuple] = None  # (lo, hi): per-request draft-token counts T_b ~ U[lo, hi]; T = hi
 
     @property
     def sm_scale(self) -> float:
@@ -203,6 +204,11 @@ CONFIGS = {
     # peaked softmax: a few planted keys score far above the rest
     "needle64k": VerifyConfig("needle64k", B=1, H=64, T=9, prefix=65536, pool_rows=1048576, nsplit=64,
                               needle=True),
+    # T = 1 decode on the verify kernels, and per-request draft-token counts
+    "decode_b16": VerifyConfig("decode_b16", B=16, H=64, T=1, prefix=(1024, 32768), pool_rows=1048576,
+                               nsplit=16),
+    "varlen_b16": VerifyConfig("varlen_b16", B=16, H=64, T=16, prefix=(1024, 32768), pool_rows=1048576,
+                               nsplit=16, T_range=(1, 16)),
 }
 
 
@@ -217,6 +223,15 @@ def make_workload(cfg: VerifyConfig, seed: Optional[int] = None, layout: Optiona
                   prefix_override: Optional[Sequence[int]] = None) -> dict:
     """Draw one verify-call input set for ``cfg`` (all arrays on the host)."""
     seed = cfg.seed if seed is None else seed
+    if cfg.T_range is not None:
+        rng = np.random.default_rng(seed + 1)
+        P = prefix_lengths(cfg, rng) if prefix_override is None else np.asarray(prefix_override, np.int64)
+        T_list = rng.integers(cfg.T_range[0], cfg.T_range[1] + 1, size=cfg.B)
+        wl = varlen_workload(cfg.B, cfg.H, T_list.tolist(), P.tolist(), cfg.pool_rows, seed, cfg.nsplit,
+                             tree=cfg.tree, layout=cfg.layout if layout is None else layout)
+        wl["cfg"] = cfg
+        wl["T"] = int(cfg.T_range[1])  # the plan's q_len bounds every T_b
+        return wl
     layout = cfg.layout if layout is None else layout
     rng = np.random.default_rng(seed)
     B, H, T = cfg.B, cfg.H, cfg.T
