@@ -13,7 +13,6 @@
 // ancestors.  Blocks of consecutive requests share bytes (a block is
 // q_len * (P_b + q_len) bits), so each thread owns whole output bytes and no
 // two threads write the same byte.
-#include "../../include/mla_verify.h"
 #include "common.cuh"
 
 namespace mlav {

@@ -85,19 +85,22 @@ def test_plan_null_pointers(lib):
     assert lib.mla_verify_destroy(None) == B.MLA_VERIFY_OK
 
 
-@pytest.mark.parametrize("H,T,flags,kernel,nq", [
-    (64, 9, 0, 1, 96),      # 576 rows -> 6 groups of 96
-    (8, 9, 0, 1, 80),       # 72 rows  -> 1 group of 80
-    (16, 4, 0, 1, 64),      # 64 rows
-    (8, 1, 0, 0, 8),        # decode with 8 heads: tile mostly padding -> CUDA cores
-    (64, 9, B.MLA_VERIFY_FORCE_SIMT, 0, 8),
+@pytest.mark.parametrize("H,T,kv,ns,flags,kernel,nq", [
+    (64, 9, 65545, 64, 0, 1, 96),  # 576 rows, 64 splits: 384 CTAs, more than one wave -> least work
+    (64, 9, 65545, 16, 0, 1, 64),  # 16 splits: 96 CTAs -> 9 x 16 = 144 fit one wave (48 rows: 192)
+    (64, 9, 5009, 16, 0, 1, 64),   # 14 splits: 84 CTAs -> 9 x 14 = 126 (48 rows: 168)
+    (64, 9, 4105, 16, 0, 1, 48),   # 11 splits: 66 CTAs -> 12 x 11 = 132
+    (8, 9, 5009, 16, 0, 1, 48),    # 72 rows: 1 group of 80 -> 2 groups of 48 (28 CTAs)
+    (16, 4, 5004, 16, 0, 1, 48),   # 64 rows -> 48 + 16
+    (8, 1, 5001, 16, 0, 0, 8),     # decode with 8 heads: tile mostly padding -> CUDA cores
+    (64, 9, 5009, 16, B.MLA_VERIFY_FORCE_SIMT, 0, 8),
 ])
-def test_plan_kernel_choice(lib, H, T, flags, kernel, nq):
-    info = plan(num_heads=H, q_len=T, max_kv_len=5000 + T, flags=flags).describe()
+def test_plan_kernel_choice(lib, H, T, kv, ns, flags, kernel, nq):
+    info = plan(num_heads=H, q_len=T, max_kv_len=kv, nsplit=ns, flags=flags).describe()
     assert info.kernel == kernel
     assert info.rows_per_cta == nq
     assert info.grid_x == -(-(H * T) // nq)
-    assert info.grid_y == 16 and info.grid_z == 1
+    assert info.grid_y == ns and info.grid_z == 1
     if kernel:
         assert 116 * 1024 < info.smem_bytes <= 227 * 1024  # one CTA per SM
 
