@@ -74,6 +74,11 @@ extern "C" {
 
 /* Plan flags. */
 #define MLA_VERIFY_FORCE_SIMT 0x1 /* use the CUDA-core (warp-shuffle) split kernel for every shape */
+/* Test only: the tensor-core split kernel's gather never signals its first
+ * block, so every CTA's bounded pipeline waits run out (about 2 s), the CTAs
+ * drain and return, and the call reports MLA_VERIFY_DEV_TIMEOUT; its outputs
+ * are not valid.  It exercises failure detection without faulting the GPU. */
+#define MLA_VERIFY_TEST_STALL_GATHER 0x100
 
 typedef struct mla_verify_plan_s* mla_verify_plan_t; /* opaque, host-only, immutable after plan */
 
@@ -86,7 +91,7 @@ typedef struct {
   int32_t nsplit;     /* >= 1: KV chunks per request = partials per output row (fixed grid dimension) */
   int32_t d_latent;   /* must be 512 */
   int32_t d_rope;     /* must be 64 */
-  int32_t flags;      /* MLA_VERIFY_FORCE_SIMT or 0 */
+  int32_t flags;      /* MLA_VERIFY_FORCE_SIMT, MLA_VERIFY_TEST_STALL_GATHER, or 0 */
 } mla_verify_params;
 
 /* What a plan chose (for tests, benchmarks and logs). */

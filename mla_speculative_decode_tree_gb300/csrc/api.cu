@@ -202,7 +202,7 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
       p.pool_rows < 1 || p.max_kv_len < p.q_len)
     return MLA_VERIFY_EINVAL;
   if (p.d_latent != kDLatent || p.d_rope != kDRope) return MLA_VERIFY_EUNSUPPORTED;
-  if ((p.flags & ~MLA_VERIFY_FORCE_SIMT) != 0) return MLA_VERIFY_EINVAL;
+  if ((p.flags & ~(MLA_VERIFY_FORCE_SIMT | MLA_VERIFY_TEST_STALL_GATHER)) != 0) return MLA_VERIFY_EINVAL;
   const int64_t rows_b = (int64_t)p.q_len * p.num_heads;
   const int64_t rows_max = rows_b * p.max_batch;
   if (rows_max > (int64_t)1 << 30 || p.pool_rows > ((int64_t)1 << 31) - 1) return MLA_VERIFY_EINVAL;
@@ -271,6 +271,7 @@ int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_
   a.mask = custom_mask;
   a.mask_indptr = mask_indptr;
   a.qo_indptr = qo_indptr;
+  a.test_stall = (pl->p.flags & MLA_VERIFY_TEST_STALL_GATHER) ? 1 : 0;
   a.batch = batch;
   a.H = pl->p.num_heads;
   a.T = pl->p.q_len;

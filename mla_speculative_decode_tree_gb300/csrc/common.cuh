@@ -33,6 +33,7 @@ struct SplitArgs {
   const int32_t* qo_indptr;      // [B+1] first token row of each request, or null: request b owns
                                  // token rows b*T .. b*T+T-1 (T = the plan's q_len, the maximum)
   int32_t batch, H, T, nsplit;
+  int32_t test_stall;            // test only: the gather never signals block 0 (waits time out)
   int64_t pool_rows;
   int64_t rows_max;              // max_batch*T*H: row stride of one split's partials
   float scale_log2;              // sm_scale * log2(e): scores are kept in base 2

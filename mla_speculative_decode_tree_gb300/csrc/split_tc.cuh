@@ -311,7 +311,9 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         stop = true;
         return;
       }
-      if (blk >= 0) {
+      if (a.test_stall && seq == 0) {
+        // test only: block 0 is never filled nor signalled
+      } else if (blk >= 0) {
         const uint32_t base = sRing + slot * Cfg::kSlotBytes + jl * 128;
         const __nv_bfloat16* src0 = a.kv_pool + blk * 64 + c8 * 8;
 #pragma unroll

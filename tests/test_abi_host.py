@@ -56,6 +56,10 @@ def test_plan_workspace_formula(lib):
     assert p.describe().workspace_bytes == p.workspace_bytes
 
 
+def test_plan_accepts_the_test_stall_flag(lib):
+    assert plan(flags=B.MLA_VERIFY_TEST_STALL_GATHER).describe().kernel == 1
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(d_latent=256), B.MLA_VERIFY_EUNSUPPORTED),
     (dict(d_rope=32), B.MLA_VERIFY_EUNSUPPORTED),
@@ -66,7 +70,7 @@ def test_plan_workspace_formula(lib):
     (dict(nsplit=0), B.MLA_VERIFY_EINVAL),
     (dict(pool_rows=0), B.MLA_VERIFY_EINVAL),
     (dict(max_kv_len=3), B.MLA_VERIFY_EINVAL),
-    (dict(flags=0x100), B.MLA_VERIFY_EINVAL),
+    (dict(flags=0x200), B.MLA_VERIFY_EINVAL),
     (dict(flags=0x2), B.MLA_VERIFY_EINVAL),
 ])
 def test_plan_rejects(lib, kw, code):
