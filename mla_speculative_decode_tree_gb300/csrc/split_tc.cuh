@@ -369,12 +369,12 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, NQ, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, NQ, true, false);
       int seq = 0;
-      bool ok = mbar_wait(&ctl.q_full, 0, &ctl.abort, a.status);
+      bool ok = mbar_wait_spin(&ctl.q_full, 0, &ctl.abort, a.status);
       // cp.async writes shared memory through the generic proxy and the MMA
       // reads it through the async proxy: a proxy fence follows each acquire.
       auto take = [&](int& slot) -> bool {
         slot = seq % S;
-        const bool r = mbar_wait(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
+        const bool r = mbar_wait_spin(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
         fence_proxy_async_smem();
         tc::fence_after_sync();
         return r;
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         if (t < nt) {
           // S^T(t) once the softmax has read S^T(t-1) out of TMEM.
           if (t >= 1) {
-            ok = mbar_wait(&ctl.s_free, (t - 1) & 1, &ctl.abort, a.status);
+            ok = mbar_wait_spin(&ctl.s_free, (t - 1) & 1, &ctl.abort, a.status);
             tc::fence_after_sync();
             if (!ok) break;
           }
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         if (t >= 1) {
           // O^T += V^T(t-1) . P^T(t-1)
           const int u = t - 1;
-          ok = mbar_wait(&ctl.p_full, u & 1, &ctl.abort, a.status);
+          ok = mbar_wait_spin(&ctl.p_full, u & 1, &ctl.abort, a.status);
           tc::fence_after_sync();
 #pragma unroll 1
           for (int m = 0; m < 4 && ok; ++m) {
