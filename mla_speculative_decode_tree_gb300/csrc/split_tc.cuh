@@ -24,7 +24,7 @@
 // tile are fetched a second time (after the next tile's key blocks) rather
 // than kept resident: a whole 128-key tile (144 KB) does not fit next to Q.
 //
-// Warp roles (up to 512 threads; CG = 3 column groups for NQ = 96, else 2):
+// Warp roles (448 or 512 threads; CG = 3 column groups for NQ = 96, else 2):
 //   warps 0..4CG-1  softmax.  Warp w reads TMEM lane quadrant w%4 (keys
 //              32(w%4)..+31 of the tile) and owns query columns
 //              [(w/4)*NQ/CG, (w/4+1)*NQ/CG).  It loads its scores once (the S^T
@@ -37,19 +37,21 @@
 //              rounding residual p - bf16(p) (completes LSE).  Epilogue: O^T
 //              scaled by 1/l and stored from TMEM straight to global memory.
 //   warp 4CG   TMEM allocation and the single MMA-issuing thread.
-//   warps 4CG+1..  gather (at most one per ring slot), taking turns block by block: cp.async 16-byte
-//              copies (from several warps: a single warp cannot issue them
-//              fast enough), rows resolved from kv_indices (prefix) or out_cache_loc
-//              (drafts) [Capture Safety to MoE Ceiling, §"The Architecture of
-//              Capture Safety"]; Q by 2-D TMA.
+//   warps 4CG+1..  gather (at most one per ring slot), taking turns block by
+//              block with 16-byte cp.async copies (several warps: one cannot
+//              issue them fast enough); rows resolved from kv_indices (prefix)
+//              or out_cache_loc (drafts, at the request's token rows)
+//              [Capture Safety to MoE Ceiling, §"The Architecture of Capture
+//              Safety"]; Q arrives once by 2-D TMA.
 // Block sequence through the ring: K(0), K(1), V(0), K(2), V(1), ...,
 // K(nt-1), V(nt-2), V(nt-1), where K(t) is the 9 column blocks of tile t and
 // V(t) its first 8 in pairs (one M=128 block of latent columns per pair).  A
 // pair must occupy adjacent slots, so an empty slot is inserted whenever a
 // pair would start in the last slot; producer and consumer apply the same rule.
 //
-// Every wait is bounded (mbar_wait); on a timeout the CTA raises the status
-// bit, all roles drain, the in-flight MMAs are awaited and TMEM is freed.
+// Every wait is bounded (mbar_wait, mbar_wait_spin for the MMA thread); on a
+// timeout the CTA raises the status bit, all roles drain, the in-flight MMAs
+// are awaited and TMEM is freed.
 #pragma once
 
 #include "common.cuh"
