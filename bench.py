@@ -72,13 +72,38 @@ def algorithmic(wl):
     return dict(rows=N, kv_bytes=N * 1152, split_bytes=split_bytes, call_bytes=call_bytes, flops=flops)
 
 
-def kernel_source_hash() -> str:
+def _strip_comments(src: str) -> str:
+    """C/C++ source without // and /* */ comments or blank space (string literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_source_hash(cdir: str = None) -> str:
+    """Hash of the kernel sources' code (comments and layout ignored): the ncu
+    counters in profiles/ stay valid across comment-only edits."""
     h = hashlib.sha256()
-    cdir = os.path.join(ROOT, "mla_speculative_decode_tree_gb300", "csrc")
+    cdir = cdir or os.path.join(ROOT, "mla_speculative_decode_tree_gb300", "csrc")
     for name in sorted(os.listdir(cdir)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(cdir, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(cdir, name), encoding="utf-8") as f:
+                h.update(name.encode() + _strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
