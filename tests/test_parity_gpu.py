@@ -73,6 +73,13 @@ ADHOC = [
     (1, 1, 16, [90], 1024, 1, "random"),             # 16 rows, one head
     (1, 32, 3, [5000], 8192, 64, "random"),          # more splits than needed: empty splits
     (2, 96, 2, [130, 129], 2048, 2, "random"),       # 192 rows = 2 x 96
+    # one case per row-group size the planner can pick (the fill-aware choice
+    # moves small grids to 48 rows, so the others need grids of >= 152 CTAs)
+    (2, 8, 4, [300, 77], 2048, 2, "random"),          # 32 rows -> 32-row groups
+    (3, 16, 4, [2000, 300, 4000], 8192, 64, "random"),  # 64 rows, 192 CTAs -> 64-row groups
+    (4, 8, 9, [3000, 100, 5000, 64], 16384, 64, "random"),  # 72 rows, 160 CTAs -> 80-row groups
+    (2, 64, 9, [5000, 3000], 16384, 64, "random"),    # 576 rows, 480 CTAs -> 96-row groups
+    (1, 2, 64, [500], 4096, 2, "random"),             # q_len 64 (the maximum): 24 tokens per group
 ]
 
 
@@ -83,6 +90,14 @@ def test_parity_adhoc(case, flags):
     wl = W.tiny_workload(B=Bn, H=H, T=T, prefix_lens=prefixes, pool_rows=pool, seed=sum(prefixes) + H,
                          tree=tree, nsplit=nsplit)
     check_full(wl, flags, what=str(case))
+
+
+def test_every_row_group_size_is_exercised():
+    sizes = set()
+    for B_, H, T, prefixes, pool, nsplit, tree in ADHOC:
+        L = max(prefixes) + T
+        sizes.add(B.mla_verify_plan(B_, H, T, L, pool, nsplit).describe().rows_per_cta)
+    assert {16, 32, 48, 64, 80, 96} <= sizes, sizes
 
 
 FULL = ["short4k", "mid64k", "long185k_h8", "batch16_ragged", "needle64k"]
