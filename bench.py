@@ -566,7 +566,7 @@ def run_reference(args):
             times.append(dt / sample * n_all * 1e6)
     us = statistics.mean(times)
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": 0,
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "what": "fp64 CPU oracle (no reference code exists to install)"},
