@@ -126,7 +126,7 @@ class ClockSampler:
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
 
     def __init__(self, gpu_index: int, log_path=None):
         self.gpu = gpu_index
@@ -185,8 +185,10 @@ class ClockSampler:
         mx = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[k] for _, p in use for k in range(4) if p[5 + k].lower().startswith("active")})
+        mem = [float(p[9]) for _, p in use if len(p) > 9 and p[9].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(during)}
+                "reasons": reasons, "mem_mhz": statistics.median(mem) if mem else None,
+                "samples": len(use), "samples_in_timed_region": len(during)}
 
 
 # ------------------------------------------------------- replica harness ----
@@ -486,6 +488,8 @@ def run_gpu(args):
         "clocks": clocks,
         "device_status": status,
         "gpu": phys.name,
+        "plan": {"kernel": "tcgen05" if info.kernel == 1 else "cuda-core", "rows_per_cta": info.rows_per_cta,
+                 "grid": [info.grid_x, info.grid_y, info.grid_z], "sm_count": phys.multi_processor_count},
     }
     if rank == 0 and not args.no_sweep:
         sweep = {}

@@ -199,13 +199,13 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
   const int nt = (int)((j1 - j0 + kKeysPerTile - 1) / kKeysPerTile);
   const int i0 = r0 / a.H;
   const int ntok = (r0 + nrows - 1) / a.H - i0 + 1;
-  // The row groups of a split read the same keys; each starts at its own
-  // tile (a rotation of the tile order) so that one group, not all of them at
-  // once, waits on the first fetch of a tile from HBM and the rest find it in
-  // L2.  The order of the tiles does not change the result beyond rounding,
-  // and it is fixed for a given grid.
-  const int groups = (rows_b + NQ - 1) / NQ;
-  const int rot = (int)(((int64_t)g * nt) / groups);
+  // The row groups of a split read the same keys; group g starts g tiles
+  // into the split (a rotation of the tile order), so the highest group
+  // fetches each tile from HBM and the others read it from L2 one or more
+  // tiles later, while it is still resident even when the keys of all splits
+  // together exceed L2.  The order of the tiles does not change the result
+  // beyond rounding, and it is fixed for a given grid.
+  const int rot = g % nt;
   auto tile_at = [&](int t) -> int { return t + rot < nt ? t + rot : t + rot - nt; };
 
   extern __shared__ uint8_t smem_raw[];
