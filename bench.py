@@ -297,6 +297,65 @@ def measure_tree_mask(torch, wl, plan, stream, steps, warmup, flush):
             "launches_per_call": 1}
 
 
+def measure_relocation(torch, name, stream, steps, warmup, flush, peaks):
+    """KV relocation (mla_verify_relocate_kv) on a verify workload whose rows sit
+    clear of a free block: µs per launch (graph-replayed, L2 flushed and the
+    original indices restored before each launch, outside the timed events),
+    GB/s of algorithmic traffic against the HBM peak, and the verify call timed
+    on the scattered rows and again on the relocated, contiguous rows (their
+    outputs must be bit-identical)."""
+    from mla_speculative_decode_tree_gb300 import binding as B
+    from mla_speculative_decode_tree_gb300 import workloads as W
+
+    wl = W.with_free_block(W.make_workload(W.CONFIGS[name]), seed=1234)
+    d = B.device_inputs(wl)
+    v = B.verifier_for(wl)
+    dst = torch.from_numpy(wl["dst_start"].astype(np.int32)).cuda()
+    idx0 = d["kv_indices"].clone()
+
+    def relocate():
+        B.mla_verify_relocate_kv(v.plan, d["kv_pool"], d["kv_indptr"], d["kv_indices"], dst, wl["B"], v.workspace,
+                                 stream=stream)
+
+    def call():
+        v.run(d, wl["B"], wl["sm_scale"], stream=stream)
+
+    g_call = capture(torch, call, stream)
+    t_before = time_graph(torch, g_call.replay, steps, warmup, flush, stream)
+    o0, l0 = v.o.clone(), v.lse.clone()
+    d["kv_indices"].copy_(idx0)
+    g_rel = capture(torch, relocate, stream)
+    times = []
+    with torch.cuda.stream(stream):
+        for it in range(warmup + steps):
+            d["kv_indices"].copy_(idx0)
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g_rel.replay()
+            e1.record(stream)
+            if it >= warmup:
+                times.append((e0, e1))
+    torch.cuda.synchronize()
+    t_rel = [a.elapsed_time(b) for a, b in times]
+    t_after = time_graph(torch, g_call.replay, steps, warmup, flush, stream)
+    same = bool(torch.equal(o0.view(torch.int16), v.o.view(torch.int16)) and torch.equal(l0, v.lse))
+    status = v.status(stream)
+    rows = int(wl["kv_indptr"][-1] - wl["kv_indptr"][0])
+    nbytes = rows * (2 * 1152 + 2 * 4) + 4 * (wl["B"] + 1) + 4 * wl["B"]
+    us = statistics.mean(t_rel) * 1e3
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del g_call, g_rel, d
+    return {"workload": name + " rows moved into a free contiguous block", "rows": rows,
+            "us": round(us, 3), "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4)},
+            "verify_us_scattered": round(statistics.mean(t_before) * 1e3, 3),
+            "verify_us_relocated": round(statistics.mean(t_after) * 1e3, 3),
+            "verify_bits_equal": same, "status": status}
+
+
 def measure_e2e(torch, wl, v, stream, steps, warmup, flush):
     """Whole call through the C ABI from pinned host memory back to pinned host memory.
 
@@ -393,8 +452,7 @@ def run_gpu(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     phys = torch.cuda.get_device_properties(local)
     gpu_index = local
-    sampler = ClockSampler(gpu_index, log_path=os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler = ClockSampler(gpu_index, log_path=args.clock_log)
     sampler.start()
     time.sleep(0.3)
 
@@ -504,6 +562,11 @@ def run_gpu(args):
                 sweep[name] = {"error": repr(exc)[:200]}
             torch.cuda.empty_cache()
         line["sweep"] = sweep
+        try:
+            line["kv_relocation"] = measure_relocation(torch, "mid64k", stream, min(args.steps, 30), 3, flush, peaks)
+        except Exception as exc:
+            line["kv_relocation"] = {"error": repr(exc)[:200]}
+        torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     if rank == 0:
@@ -628,6 +691,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="short4k")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", metavar="CSV", default=None,
+                    help="also write every nvidia-smi clock sample to this file")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="store the split kernel's DRAM bytes per launch from an ncu CSV for --workload, then exit")

@@ -242,6 +242,37 @@ int mla_verify_build_tree_mask(mla_verify_plan_t plan, const int32_t* parents, c
                                int32_t* mask_indptr, void* stream);
 
 /*
+ * KV relocation (the second, "live" tier of KV defragmentation: move each
+ * request's scattered rows into contiguous rows and rewrite its indices
+ * [The Art of Knowing When to Stop: Deferring Tier 1 Defrag, §"The Decision:
+ * Why Tier 1 Defrag Gets Deferred"]).  One kernel on `stream`, no
+ * allocation, no host synchronisation.
+ *
+ *  kv_pool      bf16 [pool_rows, 576], 16-byte aligned; read and written
+ *  kv_indptr    int32 [batch+1], non-decreasing: request b's prefix keys are
+ *               kv_indices[kv_indptr[b] .. kv_indptr[b+1])
+ *  kv_indices   int32, read and rewritten in place
+ *  dst_start    int32 [batch]: first destination row of request b
+ *  batch        0 <= batch <= max_batch (0 enqueues nothing)
+ *  workspace    the plan's workspace (only its status word is used)
+ *
+ * For every prefix key k of request b (j = k - kv_indptr[b]), pool row
+ * kv_indices[k] is copied whole to row dst_start[b] + j and kv_indices[k]
+ * becomes dst_start[b] + j.  The destination rows must be free: no source
+ * row of the call may lie in any request's destination block (the copies run
+ * in no particular order).  Draft rows (out_cache_loc) are not moved.  A key
+ * whose source or destination row is outside [0, pool_rows) is left as it was
+ * and raises MLA_VERIFY_DEV_BAD_ROW in the workspace status word.  A verify
+ * call on the relocated pool and indices gives bit-identical results (row
+ * ids do not enter the arithmetic).  The plan supplies pool_rows and the grid
+ * (max_batch x max_kv_len keys at most).  Errors: EINVAL (NULL or misaligned
+ * pointer, batch outside [0, max_batch]), EWORKSPACE, ECUDA.
+ */
+int mla_verify_relocate_kv(mla_verify_plan_t plan, void* kv_pool, const int32_t* kv_indptr, int32_t* kv_indices,
+                           const int32_t* dst_start, int32_t batch, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
  * mla_verify_run without a workspace argument, for callers that have no way
  * to obtain device memory of their own: for example a plugin host that hands
  * a kernel only its input and output buffers, or a latency-critical path that

@@ -28,7 +28,7 @@ MLA_VERIFY_TEST_STALL_GATHER = 0x100
 EXPORTED = ("mla_verify_plan", "mla_verify_plan_describe", "mla_verify_run", "mla_verify_split",
             "mla_verify_merge", "mla_verify_workspace_init", "mla_verify_read_status", "mla_verify_destroy",
             "mla_verify_strerror", "mla_verify_run_noalloc", "mla_verify_build_tree_mask",
-            "mla_verify_run_varlen")
+            "mla_verify_run_varlen", "mla_verify_relocate_kv")
 
 
 class MlaVerifyParams(ctypes.Structure):
@@ -73,6 +73,7 @@ def load(path: str = LIB_PATH):
     lib.mla_verify_run_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, i32, f32, i32, P, P, P]
     lib.mla_verify_workspace_init.argtypes = [P, P, sz, P]
     lib.mla_verify_build_tree_mask.argtypes = [P, P, P, i32, P, sz, P, P]
+    lib.mla_verify_relocate_kv.argtypes = [P, P, P, P, P, i32, P, sz, P]
     lib.mla_verify_read_status.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_verify_destroy.argtypes = [P]
     lib.mla_verify_strerror.argtypes = [ctypes.c_int]
@@ -212,6 +213,15 @@ def mla_verify_build_tree_mask(plan: Plan, parents, kv_indptr, batch: int, custo
     rc = load().mla_verify_build_tree_mask(ctypes.c_void_p(plan.handle), _ptr(parents), _ptr(kv_indptr), int(batch),
                                            _ptr(custom_mask), int(nbytes), _ptr(mask_indptr), _stream(stream))
     _check(rc, "mla_verify_build_tree_mask")
+
+
+def mla_verify_relocate_kv(plan: Plan, kv_pool, kv_indptr, kv_indices, dst_start, batch: int, workspace,
+                           stream=None):
+    """KV relocation: request b's prefix rows move to rows dst_start[b].. and kv_indices is rewritten in place."""
+    rc = load().mla_verify_relocate_kv(ctypes.c_void_p(plan.handle), _ptr(kv_pool), _ptr(kv_indptr), _ptr(kv_indices),
+                                       _ptr(dst_start), int(batch), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "mla_verify_relocate_kv")
 
 
 def mla_verify_workspace_init(plan: Plan, workspace, stream=None):

@@ -389,6 +389,24 @@ int mla_verify_build_tree_mask(mla_verify_plan_t pl, const int32_t* parents, con
   return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
 }
 
+int mla_verify_relocate_kv(mla_verify_plan_t pl, void* kv_pool, const int32_t* kv_indptr, int32_t* kv_indices,
+                           const int32_t* dst_start, int32_t batch, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (!pl || batch < 0 || batch > pl->p.max_batch) return MLA_VERIFY_EINVAL;
+  if (batch == 0) return MLA_VERIFY_OK;
+  if (!kv_pool || !kv_indptr || !kv_indices || !dst_start || !aligned(kv_pool, 16) || !aligned(kv_indptr, 4) ||
+      !aligned(kv_indices, 4) || !aligned(dst_start, 4))
+    return MLA_VERIFY_EINVAL;
+  if (!workspace || workspace_bytes < pl->ws_bytes) return MLA_VERIFY_EWORKSPACE;
+  if (!aligned(workspace, 256)) return MLA_VERIFY_EINVAL;
+  int rc;
+  if ((rc = check_device()) != MLA_VERIFY_OK) return rc;
+  const int64_t max_keys = (int64_t)pl->p.max_batch * pl->p.max_kv_len;
+  cudaError_t e = mlav::launch_relocate(kv_pool, kv_indptr, kv_indices, dst_start, batch, pl->p.pool_rows, max_keys,
+                                        reinterpret_cast<uint32_t*>(workspace), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
+}
+
 int mla_verify_workspace_init(mla_verify_plan_t pl, void* workspace, size_t workspace_bytes, void* stream) {
   if (!pl || !workspace || workspace_bytes < pl->ws_bytes || !aligned(workspace, 256)) return MLA_VERIFY_EINVAL;
   cudaError_t e = cudaMemsetAsync(workspace, 0, kWsHeader, static_cast<cudaStream_t>(stream));

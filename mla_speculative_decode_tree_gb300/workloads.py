@@ -344,6 +344,41 @@ def plant_needles(wl: dict, rng: np.random.Generator, per_request: int = 4,
     wl["needle_rows"] = np.asarray(needle_rows, dtype=np.int64)
 
 
+def with_free_block(wl: dict, seed: int) -> dict:
+    """Inputs of a KV relocation: the call's rows moved clear of a free block.
+
+    Same logical rows and queries as ``wl`` (uniform q_len), but every row the
+    call addresses is placed, scattered, at rows >= sum(P_b), so rows
+    [0, sum(P_b)) are free; ``dst_start[b]`` = kv_indptr[b] - kv_indptr[0] is
+    the contiguous destination of request b's prefix.  Unaddressed rows are
+    refilled from an independent stream.
+    """
+    assert "qo_indptr" not in wl
+    rng = np.random.default_rng(seed)
+    old_rows = logical_rows(wl)
+    n = old_rows.size
+    free = int(np.asarray(wl["prefix_lens"]).sum())
+    if free + n > wl["pool_rows"]:
+        raise ValueError("pool too small for a free block beside the call's rows")
+    new_rows = free + rng.choice(wl["pool_rows"] - free, size=n, replace=False)
+    pool = normal_bf16(np.random.default_rng(seed + 1), wl["pool"].shape)
+    pool[new_rows] = wl["pool"][old_rows]
+    out = dict(wl)
+    out["pool"] = pool
+    P = wl["prefix_lens"]
+    pos = 0
+    kv_idx, ocl = [], []
+    for b in range(wl["B"]):
+        kv_idx.append(new_rows[pos:pos + int(P[b])])
+        pos += int(P[b])
+        ocl.append(new_rows[pos:pos + wl["T"]])
+        pos += wl["T"]
+    out["kv_indices"] = np.concatenate(kv_idx).astype(np.int32) if kv_idx else np.zeros(0, np.int32)
+    out["out_cache_loc"] = np.concatenate(ocl).astype(np.int32)
+    out["dst_start"] = (wl["kv_indptr"][:-1] - wl["kv_indptr"][0]).astype(np.int32)
+    return out
+
+
 def tiny_workload(B: int, H: int, T: int, prefix_lens: Sequence[int], pool_rows: int, seed: int,
                   tree: str = "random", nsplit: int = 2) -> dict:
     """Small ad-hoc workload (same recipe) for oracle pins and edge cases."""
