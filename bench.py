@@ -236,14 +236,14 @@ def capture(torch, fn, stream):
     return g
 
 
-def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False):
+def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False, flags=0):
     from mla_speculative_decode_tree_gb300 import binding as B
     from mla_speculative_decode_tree_gb300 import workloads as W
 
     cfg = W.CONFIGS[name]
     wl = W.make_workload(cfg)
     d = B.device_inputs(wl)
-    v = B.verifier_for(wl)
+    v = B.verifier_for(wl, flags=flags)
     info = v.plan.describe()
     scale = wl["sm_scale"]
 
@@ -257,7 +257,7 @@ def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False):
 
     g_call = capture(torch, call, stream)
     t_call = time_graph(torch, g_call.replay, steps, warmup, flush, stream)
-    if "qo_indptr" in d:  # no split-only entry point for varlen calls: report the whole call
+    if "qo_indptr" in d or info.merge_blocks == 0:  # varlen or fused merge: no split-only call
         g_split, t_split = None, t_call
     else:
         g_split = capture(torch, split_only, stream)
@@ -562,6 +562,20 @@ def run_gpu(args):
                 sweep[name] = {"error": repr(exc)[:200]}
             torch.cuda.empty_cache()
         line["sweep"] = sweep
+        fused = {}
+        for name in ("short4k", "mid64k", "decode_b16"):
+            try:
+                res = measure_workload(torch, name, min(args.steps, 30), 3, flush, stream,
+                                       flags=B.MLA_VERIFY_FUSED_MERGE)
+                fused[name] = {"us_per_call": round(statistics.mean(res["t_call"]) * 1e3, 3),
+                               "separate_merge_us_per_call": (us_call if name == args.workload else
+                                                              sweep.get(name, {}).get("us_per_call")),
+                               "status": res["status"]}
+                del res
+            except Exception as exc:
+                fused[name] = {"error": repr(exc)[:200]}
+            torch.cuda.empty_cache()
+        line["fused_merge"] = fused
         try:
             line["kv_relocation"] = measure_relocation(torch, "mid64k", stream, min(args.steps, 30), 3, flush, peaks)
         except Exception as exc:

@@ -74,6 +74,14 @@ extern "C" {
 
 /* Plan flags. */
 #define MLA_VERIFY_FORCE_SIMT 0x1 /* use the CUDA-core (warp-shuffle) split kernel for every shape */
+/* Merge inside the tensor-core split kernel: the last CTA of each (request,
+ * row group) to finish merges that group's rows from the other CTAs'
+ * partials, so a run is one kernel launch (describe() then reports
+ * merge_blocks = 0).  Results are bit-identical to the separate merge.  The
+ * workspace gains one counter per (request, row group) between the header
+ * and the partials; mla_verify_split is refused (EINVAL) for such a plan.
+ * Ignored when the plan picks the CUDA-core kernel. */
+#define MLA_VERIFY_FUSED_MERGE 0x2
 /* Test only: the tensor-core split kernel's gather never signals its first
  * block, so every CTA's bounded pipeline waits run out (about 2 s), the CTAs
  * drain and return, and the call reports MLA_VERIFY_DEV_TIMEOUT; its outputs
@@ -91,7 +99,7 @@ typedef struct {
   int32_t nsplit;     /* >= 1: KV chunks per request = partials per output row (fixed grid dimension) */
   int32_t d_latent;   /* must be 512 */
   int32_t d_rope;     /* must be 64 */
-  int32_t flags;      /* MLA_VERIFY_FORCE_SIMT, MLA_VERIFY_TEST_STALL_GATHER, or 0 */
+  int32_t flags;      /* OR of MLA_VERIFY_FORCE_SIMT, MLA_VERIFY_FUSED_MERGE, MLA_VERIFY_TEST_STALL_GATHER */
 } mla_verify_params;
 
 /* What a plan chose (for tests, benchmarks and logs). */
@@ -100,7 +108,7 @@ typedef struct {
   int32_t rows_per_cta;  /* query rows (token x head pairs) one split CTA covers */
   int32_t keys_per_tile; /* keys per pipeline tile (chunk sizes are multiples of it) */
   int32_t grid_x, grid_y, grid_z; /* split grid: row groups x nsplit x max_batch */
-  int32_t merge_blocks;  /* merge grid size */
+  int32_t merge_blocks;  /* merge grid size; 0 when the split kernel merges (MLA_VERIFY_FUSED_MERGE) */
   int32_t smem_bytes;    /* dynamic shared memory of the split kernel */
   size_t workspace_bytes;
 } mla_verify_plan_info;
@@ -109,10 +117,12 @@ typedef struct {
  * Validate `params` and build a plan.  Host only: touches no device state.
  * On success *out receives the plan and *workspace_bytes the size of the
  * device workspace every run with this plan needs (fp32 partial O and LSE
- * for nsplit x max_batch*q_len*num_heads rows plus a 256-byte header).
+ * for nsplit x max_batch*q_len*num_heads rows plus a 256-byte header, and
+ * for MLA_VERIFY_FUSED_MERGE one 32-bit counter per request and row group).
  * The workspace must be 256-byte aligned and zero-filled once before its
  * first use (e.g. torch.zeros, or mla_verify_workspace_init); the library
- * keeps the header consistent afterwards.
+ * keeps the header and the counters consistent afterwards (after a call that
+ * reported MLA_VERIFY_DEV_TIMEOUT, initialise it again).
  * Errors: EINVAL (NULL pointer, non-positive sizes, q_len > 64),
  * EUNSUPPORTED (d_latent != 512 or d_rope != 64).
  */
@@ -187,7 +197,9 @@ int mla_verify_run_varlen(mla_verify_plan_t plan, const void* q_nope_absorbed, c
  * the partials into the workspace) and the merge kernel (reads them, writes
  * o and lse).  Same arguments and errors as mla_verify_run; merge ignores
  * the input arrays.  A merge must follow the split of the same call on the
- * same stream (or be ordered after it).
+ * same stream (or be ordered after it).  A plan with MLA_VERIFY_FUSED_MERGE
+ * on the tensor-core kernel has no split-only call (EINVAL); merge still
+ * works on the partials its run left in the workspace.
  */
 int mla_verify_split(mla_verify_plan_t plan, const void* q_nope_absorbed, const void* q_rope,
                      const void* kv_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
@@ -197,7 +209,8 @@ int mla_verify_split(mla_verify_plan_t plan, const void* q_nope_absorbed, const 
 int mla_verify_merge(mla_verify_plan_t plan, int32_t batch, int32_t nsplit, void* workspace,
                      size_t workspace_bytes, void* o, float* lse, void* stream);
 
-/* Zero the workspace header on `stream` (one cudaMemsetAsync).  Errors: EINVAL, ECUDA. */
+/* Zero the workspace header (and a fused merge's counters) on `stream` (one
+ * cudaMemsetAsync).  Errors: EINVAL, ECUDA. */
 int mla_verify_workspace_init(mla_verify_plan_t plan, void* workspace, size_t workspace_bytes,
                               void* stream);
 

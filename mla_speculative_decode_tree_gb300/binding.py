@@ -23,6 +23,7 @@ MLA_VERIFY_ECUDA = 4
 MLA_VERIFY_DEV_BAD_ROW = 0x1
 MLA_VERIFY_DEV_TIMEOUT = 0x2
 MLA_VERIFY_FORCE_SIMT = 0x1
+MLA_VERIFY_FUSED_MERGE = 0x2
 MLA_VERIFY_TEST_STALL_GATHER = 0x100
 
 EXPORTED = ("mla_verify_plan", "mla_verify_plan_describe", "mla_verify_run", "mla_verify_split",

@@ -20,7 +20,8 @@ struct mla_verify_plan_s {
   int nq;      // query rows per split CTA
   int groups;  // row groups per request
   int64_t rows_max;
-  size_t off_lse, off_o, ws_bytes;
+  bool fused;  // the split kernel merges (MLA_VERIFY_FUSED_MERGE on the tensor-core kernel)
+  size_t off_cnt, off_lse, off_o, ws_bytes;  // [0, off_lse) must be zero between calls
   int merge_blocks;
   int smem;
 };
@@ -191,6 +192,9 @@ namespace mlav {
 // Records the text of a CUDA error for mla_verify_strerror (used by other
 // translation units of the library) and returns MLA_VERIFY_ECUDA.
 int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+// Bytes at the start of a plan's workspace that must be zero between calls
+// (status header and, for a fused merge, the arrival counters).
+size_t plan_zero_bytes(const mla_verify_plan_s* pl) { return pl->off_lse; }
 }  // namespace mlav
 
 extern "C" {
@@ -202,7 +206,8 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
       p.pool_rows < 1 || p.max_kv_len < p.q_len)
     return MLA_VERIFY_EINVAL;
   if (p.d_latent != kDLatent || p.d_rope != kDRope) return MLA_VERIFY_EUNSUPPORTED;
-  if ((p.flags & ~(MLA_VERIFY_FORCE_SIMT | MLA_VERIFY_TEST_STALL_GATHER)) != 0) return MLA_VERIFY_EINVAL;
+  if ((p.flags & ~(MLA_VERIFY_FORCE_SIMT | MLA_VERIFY_FUSED_MERGE | MLA_VERIFY_TEST_STALL_GATHER)) != 0)
+    return MLA_VERIFY_EINVAL;
   const int64_t rows_b = (int64_t)p.q_len * p.num_heads;
   const int64_t rows_max = rows_b * p.max_batch;
   if (rows_max > (int64_t)1 << 30 || p.pool_rows > ((int64_t)1 << 31) - 1) return MLA_VERIFY_EINVAL;
@@ -218,10 +223,13 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
   pl->groups = (int)((rows_b + pl->nq - 1) / pl->nq);
   pl->smem = pl->kernel ? tc_smem(pl->nq) : 0;
 
-  pl->off_lse = kWsHeader;
+  pl->fused = pl->kernel == 1 && (p.flags & MLA_VERIFY_FUSED_MERGE);
+  pl->off_cnt = kWsHeader;
+  pl->off_lse = pl->fused ? round_up(pl->off_cnt + sizeof(uint32_t) * (size_t)p.max_batch * pl->groups, 256)
+                          : kWsHeader;
   pl->off_o = round_up(pl->off_lse + sizeof(float) * (size_t)p.nsplit * (size_t)rows_max, 256);
   pl->ws_bytes = pl->off_o + sizeof(float) * (size_t)p.nsplit * (size_t)rows_max * kDLatent;
-  pl->merge_blocks = merge_blocks((int)rows_max);
+  pl->merge_blocks = pl->fused ? 0 : merge_blocks((int)rows_max);
   *workspace_bytes = pl->ws_bytes;
   *out = pl;
   return MLA_VERIFY_OK;
@@ -248,9 +256,11 @@ namespace {
 int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_rope, const void* kv_pool,
                const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* qo_indptr,
                const int32_t* out_cache_loc, const uint8_t* custom_mask, const int32_t* mask_indptr, int32_t batch,
-               float sm_scale, int32_t nsplit, void* workspace, size_t workspace_bytes, void* stream) {
+               float sm_scale, int32_t nsplit, void* workspace, size_t workspace_bytes, void* o, float* lse,
+               void* stream) {
   int rc = check_common(pl, batch, nsplit, workspace, workspace_bytes);
   if (rc != MLA_VERIFY_OK || batch == 0) return rc;
+  if (pl->fused && (!o || !lse)) return MLA_VERIFY_EINVAL;  // a fused plan has no split-only call
   if (!q_nope_absorbed || !q_rope || !kv_pool || !kv_indptr || !out_cache_loc || !custom_mask || !mask_indptr)
     return MLA_VERIFY_EINVAL;
   // kv_indices may be NULL only when every prefix is empty; the device never
@@ -283,6 +293,9 @@ int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.part_lse = reinterpret_cast<float*>(ws + pl->off_lse);
   a.part_o = reinterpret_cast<float*>(ws + pl->off_o);
+  a.merge_count = pl->fused ? reinterpret_cast<uint32_t*>(ws + pl->off_cnt) : nullptr;
+  a.o = pl->fused ? static_cast<__nv_bfloat16*>(o) : nullptr;
+  a.lse = pl->fused ? lse : nullptr;
 
   const dim3 grid(pl->groups, pl->p.nsplit, pl->p.max_batch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -337,7 +350,7 @@ int mla_verify_split(mla_verify_plan_t pl, const void* q_nope_absorbed, const vo
                      const uint8_t* custom_mask, const int32_t* mask_indptr, int32_t batch, float sm_scale,
                      int32_t nsplit, void* workspace, size_t workspace_bytes, void* stream) {
   return split_impl(pl, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, nullptr, out_cache_loc, custom_mask,
-                    mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, stream);
+                    mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, nullptr, nullptr, stream);
 }
 
 int mla_verify_merge(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, void* workspace, size_t workspace_bytes,
@@ -353,8 +366,8 @@ int mla_verify_run(mla_verify_plan_t pl, const void* q_nope_absorbed, const void
   if (rc != MLA_VERIFY_OK || batch == 0) return rc;
   if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return MLA_VERIFY_EINVAL;
   rc = split_impl(pl, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, nullptr, out_cache_loc, custom_mask,
-                  mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, stream);
-  if (rc != MLA_VERIFY_OK) return rc;
+                  mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, o, lse, stream);
+  if (rc != MLA_VERIFY_OK || pl->fused) return rc;
   return merge_impl(pl, batch, nsplit, nullptr, workspace, workspace_bytes, o, lse, stream);
 }
 
@@ -368,8 +381,8 @@ int mla_verify_run_varlen(mla_verify_plan_t pl, const void* q_nope_absorbed, con
   if (!qo_indptr || !aligned(qo_indptr, 4)) return MLA_VERIFY_EINVAL;
   if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return MLA_VERIFY_EINVAL;
   rc = split_impl(pl, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, qo_indptr, out_cache_loc,
-                  custom_mask, mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, stream);
-  if (rc != MLA_VERIFY_OK) return rc;
+                  custom_mask, mask_indptr, batch, sm_scale, nsplit, workspace, workspace_bytes, o, lse, stream);
+  if (rc != MLA_VERIFY_OK || pl->fused) return rc;
   return merge_impl(pl, batch, nsplit, qo_indptr, workspace, workspace_bytes, o, lse, stream);
 }
 
@@ -409,7 +422,7 @@ int mla_verify_relocate_kv(mla_verify_plan_t pl, void* kv_pool, const int32_t* k
 
 int mla_verify_workspace_init(mla_verify_plan_t pl, void* workspace, size_t workspace_bytes, void* stream) {
   if (!pl || !workspace || workspace_bytes < pl->ws_bytes || !aligned(workspace, 256)) return MLA_VERIFY_EINVAL;
-  cudaError_t e = cudaMemsetAsync(workspace, 0, kWsHeader, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaMemsetAsync(workspace, 0, pl->off_lse, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
 }
 

@@ -40,6 +40,12 @@ struct SplitArgs {
   float* part_lse;               // [nsplit, rows_max]   natural log, -inf when nothing visible
   float* part_o;                 // [nsplit, rows_max, 512] normalised partial output
   uint32_t* status;              // workspace header word 0
+  // Fused merge (tensor-core kernel only; null when the merge kernel runs):
+  // one arrival counter per (request, row group), zero between calls, and the
+  // final outputs the last CTA of a group writes.
+  uint32_t* merge_count;         // [max_batch, groups]
+  __nv_bfloat16* o;              // [rows, 512]
+  float* lse;                    // [rows]
 };
 
 // TMA descriptors of one call: the pool for row gathers (box 64 columns x 1

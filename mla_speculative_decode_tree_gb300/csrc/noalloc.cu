@@ -10,6 +10,7 @@
 
 namespace mlav {
 int record_cuda_error(cudaError_t e);  // api.cu: keeps the text for mla_verify_strerror
+size_t plan_zero_bytes(const mla_verify_plan_s* pl);  // api.cu: header + merge counters
 }
 
 namespace {
@@ -53,9 +54,10 @@ extern "C" int mla_verify_run_noalloc(mla_verify_plan_t plan, const void* q_nope
   if (info.workspace_bytes > kNoAllocScratchBytes) return MLA_VERIFY_EWORKSPACE;
   void* scratch = nullptr;
   if ((rc = scratch_for_current_device(&scratch)) != MLA_VERIFY_OK) return rc;
-  // The array keeps the previous call's contents; its status header must
-  // start at zero for this call (the partials are rewritten in full).
-  cudaError_t e = cudaMemsetAsync(scratch, 0, mlav::kWsHeader, static_cast<cudaStream_t>(stream));
+  // The array keeps the previous call's contents; its status header (and a
+  // fused merge's counters) must start at zero for this call (the partials
+  // are rewritten in full).
+  cudaError_t e = cudaMemsetAsync(scratch, 0, mlav::plan_zero_bytes(plan), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return mlav::record_cuda_error(e);
   return mla_verify_run(plan, q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, out_cache_loc, custom_mask,
                         mask_indptr, batch, sm_scale, nsplit, scratch, kNoAllocScratchBytes, o, lse, stream);

@@ -55,6 +55,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "merge_row.cuh"
 #include "tc_ptx.cuh"
 
 namespace mlav {
@@ -98,6 +99,7 @@ struct TcCtl {
   uint64_t q_full, s_full, s_free, p_full, pv_done[2], mma_idle;
   uint32_t tmem_base;
   int abort;
+  int merge_last;  // fused merge: this CTA is the last of its row group to finish
   int flag[2][12];
   int rflag[2];
   alignas(16) float mtau[NQ];   // running max + kTau (base 2); -inf before any visible key
@@ -159,7 +161,9 @@ __device__ __forceinline__ void warp_columns_to_smem(const float (&x)[HC], float
   }
 }
 
-template <int NQ>
+// kFused: the CTA that finishes a row group last also merges it (a separate
+// instantiation, so the plain kernel carries none of that code).
+template <int NQ, bool kFused>
 __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     split_tc_kernel(const __grid_constant__ SplitArgs a, const __grid_constant__ TcMaps maps) {
   using Cfg = TcCfg<NQ>;
@@ -666,13 +670,38 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
+
+  // ---- fused merge ------------------------------------------------------------
+  // Every CTA of a (request, row group) takes a ticket once its partials are
+  // visible device-wide; the one that takes the last ticket (of the
+  // request's non-empty splits) merges the group's rows and resets the
+  // counter for the next call.  Nobody waits on another CTA.
+  if constexpr (kFused) {
+    const int n_split = (int)((L + chunk - 1) / chunk);  // splits with keys: 0..n_split-1
+    uint32_t* cnt = a.merge_count + (int64_t)b * gridDim.x + g;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const bool last = atomicAdd(cnt, 1u) + 1u == (uint32_t)n_split;
+      if (last) *cnt = 0u;
+      ctl.merge_last = last ? 1 : 0;
+    }
+    __syncthreads();
+    if (ctl.merge_last) {
+      __threadfence();
+      // warp w merges half w%2 of row w/2, then of row (w + warps)/2, ...
+      for (int w = warp; w < 2 * nrows; w += kTcThreads / 32)
+        merge_row_half<true>(a.part_lse, a.part_o, a.rows_max, n_split, grow0 + (w >> 1), w & 1, lane, a.o, a.lse);
+    }
+  }
 }
 
 template <int NQ>
 cudaError_t launch_split_tc_nq(const SplitArgs& a, const TcMaps& maps, dim3 grid, cudaStream_t stream) {
   constexpr int smem = tc_smem_bytes<NQ>();
   static_assert(smem <= 232448, "shared memory budget exceeded");
-  cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  void (*kernel)(SplitArgs, TcMaps) = a.merge_count ? split_tc_kernel<NQ, true> : split_tc_kernel<NQ, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -681,7 +710,7 @@ cudaError_t launch_split_tc_nq(const SplitArgs& a, const TcMaps& maps, dim3 grid
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  e = cudaLaunchKernelEx(&cfg, split_tc_kernel<NQ>, a, maps);
+  e = cudaLaunchKernelEx(&cfg, kernel, a, maps);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

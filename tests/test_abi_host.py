@@ -56,6 +56,25 @@ def test_plan_workspace_formula(lib):
     assert p.describe().workspace_bytes == p.workspace_bytes
 
 
+def test_fused_merge_plan(lib):
+    """The counters sit between the header and the partials; no merge grid; the
+    flag is ignored by the CUDA-core kernel; no split-only call."""
+    p = plan(max_batch=2, nsplit=16, flags=B.MLA_VERIFY_FUSED_MERGE)
+    info = p.describe()
+    assert info.kernel == 1 and info.merge_blocks == 0
+    rows = 2 * 9 * 64
+    off_lse = (256 + 4 * 2 * info.grid_x + 255) // 256 * 256
+    off_o = (off_lse + 4 * 16 * rows + 255) // 256 * 256
+    assert p.workspace_bytes == off_o + 4 * 16 * rows * 512
+    simt = plan(num_heads=2, q_len=4, flags=B.MLA_VERIFY_FUSED_MERGE)
+    assert simt.describe().kernel == 0 and simt.describe().merge_blocks > 0
+    assert simt.workspace_bytes == plan(num_heads=2, q_len=4).workspace_bytes
+    ptr = FAKE
+    rc = lib.mla_verify_split(ctypes.c_void_p(p.handle), ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 0.072, 16, FAKE,
+                              p.workspace_bytes, None)
+    assert rc == B.MLA_VERIFY_EINVAL
+
+
 def test_plan_accepts_the_test_stall_flag(lib):
     assert plan(flags=B.MLA_VERIFY_TEST_STALL_GATHER).describe().kernel == 1
 
@@ -71,7 +90,7 @@ def test_plan_accepts_the_test_stall_flag(lib):
     (dict(pool_rows=0), B.MLA_VERIFY_EINVAL),
     (dict(max_kv_len=3), B.MLA_VERIFY_EINVAL),
     (dict(flags=0x200), B.MLA_VERIFY_EINVAL),
-    (dict(flags=0x2), B.MLA_VERIFY_EINVAL),
+    (dict(flags=0x4), B.MLA_VERIFY_EINVAL),
 ])
 def test_plan_rejects(lib, kw, code):
     with pytest.raises(B.MlaVerifyError) as e:
