@@ -418,7 +418,8 @@ def summarize(res, peaks):
     t_hbm = alg["call_bytes"] / hbm * 1e6
     t_mma = alg["flops"] / mma * 1e6
     return dict(
-        us_per_call=t_call_us, us_p10=float(np.percentile(res["t_call"], 10) * 1e3),
+        us_per_call=t_call_us, us_median=float(np.median(res["t_call"]) * 1e3),
+        us_p10=float(np.percentile(res["t_call"], 10) * 1e3),
         us_p90=float(np.percentile(res["t_call"], 90) * 1e3), split_us=t_split_us,
         gathered_kv_gbs=alg["kv_bytes"] / (t_call_us * 1e-6) / 1e9,
         tflops=alg["flops"] / (t_call_us * 1e-6) / 1e12,
@@ -535,6 +536,9 @@ def run_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "l2": "flushed (512 MiB write) before every step",
                    "parallelism": "replicas" if world > 1 else "single GPU", "graph": "split+merge in one CUDA graph"},
+        "us_per_call_median": round(float(np.median(step_ms)) * 1e3, 3),
+        "us_per_call_p10_p90": [round(float(np.percentile(step_ms, 10)) * 1e3, 3),
+                                round(float(np.percentile(step_ms, 90)) * 1e3, 3)],
         "gathered_kv_gbs": round(alg["kv_bytes"] / (us_call * world * 1e-6) / 1e9, 2),
         "roofline_frac_call": round(max(t_hbm_us, t_mma_us) / (us_call * world), 4),
         "roofline": roofline,
@@ -617,11 +621,17 @@ def cpu_baseline(wl, budget_s=15.0, rows=None):
         reps += more
         dt = time.perf_counter() - t0
     us_call = dt / reps / rows.size * n_all * 1e6
+    # the same oracle on one core, on a few rows, scaled to a whole call
+    few = np.sort(rng.choice(n_all, size=min(n_all, 16), replace=False))
+    t1 = time.perf_counter()
+    ref.verify(wl, rows=few, nthreads=1)
+    us_call_1 = (time.perf_counter() - t1) / few.size * n_all * 1e6
     if reps > 1:
         sample = "%d whole calls (all %d output rows each), fp64, %.1f s wall" % (reps, n_all, dt)
     else:
         sample = "%d of %d output rows (token x head) of the workload, fp64, %.1f s wall" % (rows.size, n_all, dt)
-    return {"value": round(us_call, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    return {"value": round(us_call, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+            "value_1core": round(us_call_1, 1), "sample_1core": "%d rows on 1 thread, scaled" % few.size}
 
 
 def run_reference(args):
