@@ -572,8 +572,8 @@ def run_gpu(args):
                 res = measure_workload(torch, name, min(args.steps, 30), 3, flush, stream,
                                        flags=B.MLA_VERIFY_FUSED_MERGE)
                 fused[name] = {"us_per_call": round(statistics.mean(res["t_call"]) * 1e3, 3),
-                               "separate_merge_us_per_call": (us_call if name == args.workload else
-                                                              sweep.get(name, {}).get("us_per_call")),
+                               "separate_merge_us_per_call": round(us_call, 3) if name == args.workload else
+                               sweep.get(name, {}).get("us_per_call"),
                                "status": res["status"]}
                 del res
             except Exception as exc:
