@@ -720,6 +720,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="store the split kernel's DRAM bytes per launch from an ncu CSV for --workload, then exit")
+    ap.add_argument("--relocation-only", action="store_true",
+                    help="time only the KV relocation call on --workload's rows (steps/warmup as given)")
     args = ap.parse_args(argv)
     if args.record_traffic:
         print(json.dumps(record_traffic(args.record_traffic, args.workload)))
@@ -728,6 +730,14 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.relocation_only:
+        import torch
+        from __graft_entry__ import build
+        build()
+        peaks, _ = load_peaks()
+        stream = torch.cuda.Stream()
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        print(json.dumps(measure_relocation(torch, args.workload, stream, args.steps, args.warmup, flush, peaks)))
     else:
         run_gpu(args)
 
