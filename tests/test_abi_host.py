@@ -153,3 +153,24 @@ def test_run_host_validation(lib):
     assert lib.mla_verify_merge(ctypes.c_void_p(p.handle), 3, p.nsplit, FAKE, p.workspace_bytes, FAKE, FAKE,
                                 None) == B.MLA_VERIFY_EINVAL
     assert lib.mla_verify_workspace_init(ctypes.c_void_p(p.handle), FAKE, 16, None) == B.MLA_VERIFY_EINVAL
+
+
+def test_relocate_host_validation(lib):
+    p = plan(max_batch=2)
+    h = ctypes.c_void_p(p.handle)
+
+    def call(pool=FAKE, indptr=FAKE, idx=FAKE, dst=FAKE, batch=1, ws=FAKE, ws_bytes=None):
+        return lib.mla_verify_relocate_kv(h, pool, indptr, idx, dst, batch, ws,
+                                          p.workspace_bytes if ws_bytes is None else ws_bytes, None)
+
+    assert call(batch=0) == B.MLA_VERIFY_OK
+    assert call(batch=3) == B.MLA_VERIFY_EINVAL
+    assert call(batch=-1) == B.MLA_VERIFY_EINVAL
+    assert call(pool=None) == B.MLA_VERIFY_EINVAL
+    assert call(dst=None) == B.MLA_VERIFY_EINVAL
+    assert call(pool=FAKE + 8) == B.MLA_VERIFY_EINVAL       # pool not 16-byte aligned
+    assert call(idx=FAKE + 2) == B.MLA_VERIFY_EINVAL        # indices not 4-byte aligned
+    assert call(ws=None) == B.MLA_VERIFY_EWORKSPACE
+    assert call(ws_bytes=p.workspace_bytes - 1) == B.MLA_VERIFY_EWORKSPACE
+    assert call(ws=FAKE + 16) == B.MLA_VERIFY_EINVAL        # workspace not 256-byte aligned
+    assert lib.mla_verify_relocate_kv(None, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1 << 30, None) == B.MLA_VERIFY_EINVAL
