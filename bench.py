@@ -265,9 +265,7 @@ def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False, 
     status = v.status(stream)
     alg = algorithmic(wl)
     res = dict(wl=wl, info=info, t_call=t_call, t_split=t_split, alg=alg, status=status,
-               # the device tree-mask builder serves uniform q_len calls
-               tree_mask=None if "qo_indptr" in d else measure_tree_mask(torch, wl, v.plan, stream, steps, warmup,
-                                                                         flush))
+               tree_mask=measure_tree_mask(torch, wl, v.plan, stream, steps, warmup, flush))
     if with_e2e:
         res["e2e"] = measure_e2e(torch, wl, v, stream, steps, warmup, flush)
     del g_call, g_split, d
@@ -285,12 +283,17 @@ def measure_tree_mask(torch, wl, plan, stream, steps, warmup, flush):
     mip = torch.zeros_like(dev["mask_indptr"])
 
     def build():
-        B.mla_verify_build_tree_mask(plan, parents, dev["kv_indptr"], wl["B"], mask, mip, stream=stream)
+        if "qo_indptr" in dev:
+            B.mla_verify_build_tree_mask_varlen(plan, parents, dev["kv_indptr"], dev["qo_indptr"], wl["B"], mask, mip,
+                                                stream=stream)
+        else:
+            B.mla_verify_build_tree_mask(plan, parents, dev["kv_indptr"], wl["B"], mask, mip, stream=stream)
 
     g = capture(torch, build, stream)
     t = time_graph(torch, g.replay, steps, warmup, flush, stream)
     torch.cuda.synchronize()
-    n = (wl["T"] * int(sum(int(p) + wl["T"] for p in wl["prefix_lens"])) + 7) // 8
+    counts = wl["T_list"] if wl.get("T_list") is not None else [wl["T"]] * wl["B"]
+    n = (int(sum(int(t_b) * (int(p) + int(t_b)) for p, t_b in zip(wl["prefix_lens"], counts))) + 7) // 8
     same = bool(torch.equal(mask[:n], dev["custom_mask"][:n]) and torch.equal(mip, dev["mask_indptr"]))
     del g
     return {"us": round(statistics.mean(t) * 1e3, 3), "mask_bytes": n, "matches_input_mask": same,

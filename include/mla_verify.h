@@ -255,6 +255,19 @@ int mla_verify_build_tree_mask(mla_verify_plan_t plan, const int32_t* parents, c
                                int32_t* mask_indptr, void* stream);
 
 /*
+ * mla_verify_build_tree_mask for a varlen call (see mla_verify_run_varlen):
+ * request b has T_b = qo_indptr[b+1] - qo_indptr[b] draft tokens
+ * (0 <= T_b <= q_len), its parent array is parents[qo_indptr[b] ..
+ * qo_indptr[b] + T_b) (node indices local to the request, -1 for a root),
+ * its block is [T_b, P_b + T_b] and mask_indptr[b] =
+ * sum_{b'<b} T_b' * (P_b' + T_b').  Other arguments and the bit rule as
+ * mla_verify_build_tree_mask.  Errors: EINVAL (also batch > 1024), ECUDA.
+ */
+int mla_verify_build_tree_mask_varlen(mla_verify_plan_t plan, const int32_t* parents, const int32_t* kv_indptr,
+                                      const int32_t* qo_indptr, int32_t batch, uint8_t* custom_mask,
+                                      size_t mask_bytes, int32_t* mask_indptr, void* stream);
+
+/*
  * KV relocation (the second, "live" tier of KV defragmentation: move each
  * request's scattered rows into contiguous rows and rewrite its indices
  * [The Art of Knowing When to Stop: Deferring Tier 1 Defrag, §"The Decision:

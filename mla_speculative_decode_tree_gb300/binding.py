@@ -29,7 +29,7 @@ MLA_VERIFY_TEST_STALL_GATHER = 0x100
 EXPORTED = ("mla_verify_plan", "mla_verify_plan_describe", "mla_verify_run", "mla_verify_split",
             "mla_verify_merge", "mla_verify_workspace_init", "mla_verify_read_status", "mla_verify_destroy",
             "mla_verify_strerror", "mla_verify_run_noalloc", "mla_verify_build_tree_mask",
-            "mla_verify_run_varlen", "mla_verify_relocate_kv")
+            "mla_verify_run_varlen", "mla_verify_relocate_kv", "mla_verify_build_tree_mask_varlen")
 
 
 class MlaVerifyParams(ctypes.Structure):
@@ -75,6 +75,7 @@ def load(path: str = LIB_PATH):
     lib.mla_verify_workspace_init.argtypes = [P, P, sz, P]
     lib.mla_verify_build_tree_mask.argtypes = [P, P, P, i32, P, sz, P, P]
     lib.mla_verify_relocate_kv.argtypes = [P, P, P, P, P, i32, P, sz, P]
+    lib.mla_verify_build_tree_mask_varlen.argtypes = [P, P, P, P, i32, P, sz, P, P]
     lib.mla_verify_read_status.argtypes = [P, P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_verify_destroy.argtypes = [P]
     lib.mla_verify_strerror.argtypes = [ctypes.c_int]
@@ -223,6 +224,17 @@ def mla_verify_relocate_kv(plan: Plan, kv_pool, kv_indptr, kv_indices, dst_start
                                        _ptr(dst_start), int(batch), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "mla_verify_relocate_kv")
+
+
+def mla_verify_build_tree_mask_varlen(plan: Plan, parents, kv_indptr, qo_indptr, batch: int, custom_mask,
+                                      mask_indptr, stream=None, mask_bytes: Optional[int] = None):
+    """Device tree-mask build for a varlen call: parents int32 [qo_indptr[batch]] (request b's at
+    qo_indptr[b]..), blocks [T_b, P_b + T_b]."""
+    nbytes = custom_mask.numel() * custom_mask.element_size() if mask_bytes is None else mask_bytes
+    rc = load().mla_verify_build_tree_mask_varlen(ctypes.c_void_p(plan.handle), _ptr(parents), _ptr(kv_indptr),
+                                                  _ptr(qo_indptr), int(batch), _ptr(custom_mask), int(nbytes),
+                                                  _ptr(mask_indptr), _stream(stream))
+    _check(rc, "mla_verify_build_tree_mask_varlen")
 
 
 def mla_verify_workspace_init(plan: Plan, workspace, stream=None):

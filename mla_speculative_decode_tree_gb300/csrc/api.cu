@@ -397,8 +397,24 @@ int mla_verify_build_tree_mask(mla_verify_plan_t pl, const int32_t* parents, con
   int rc;
   if ((rc = check_device()) != MLA_VERIFY_OK) return rc;
   const int64_t max_bytes = ((int64_t)pl->p.max_batch * pl->p.q_len * pl->p.max_kv_len + 7) / 8;
-  cudaError_t e = launch_tree_mask(parents, kv_indptr, batch, pl->p.q_len, custom_mask, (int64_t)mask_bytes,
+  cudaError_t e = launch_tree_mask(parents, kv_indptr, nullptr, batch, pl->p.q_len, custom_mask, (int64_t)mask_bytes,
                                    mask_indptr, max_bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
+}
+
+int mla_verify_build_tree_mask_varlen(mla_verify_plan_t pl, const int32_t* parents, const int32_t* kv_indptr,
+                                      const int32_t* qo_indptr, int32_t batch, uint8_t* custom_mask,
+                                      size_t mask_bytes, int32_t* mask_indptr, void* stream) {
+  if (!pl || batch < 0 || batch > pl->p.max_batch || batch > kMaxTreeMaskVarlenBatch) return MLA_VERIFY_EINVAL;
+  if (batch == 0) return MLA_VERIFY_OK;
+  if (!parents || !kv_indptr || !qo_indptr || !custom_mask || !mask_indptr || !aligned(parents, 4) ||
+      !aligned(kv_indptr, 4) || !aligned(qo_indptr, 4) || !aligned(mask_indptr, 4))
+    return MLA_VERIFY_EINVAL;
+  int rc;
+  if ((rc = check_device()) != MLA_VERIFY_OK) return rc;
+  const int64_t max_bytes = ((int64_t)pl->p.max_batch * pl->p.q_len * pl->p.max_kv_len + 7) / 8;
+  cudaError_t e = launch_tree_mask(parents, kv_indptr, qo_indptr, batch, pl->p.q_len, custom_mask,
+                                   (int64_t)mask_bytes, mask_indptr, max_bytes, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
 }
 

@@ -233,8 +233,10 @@ MLAV_DECLARE_TC(80)
 MLAV_DECLARE_TC(96)
 #undef MLAV_DECLARE_TC
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
-cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* kv_indptr, int batch, int T, uint8_t* mask,
-                             int64_t mask_bytes, int32_t* mask_indptr, int64_t max_bytes, cudaStream_t stream);
+constexpr int kMaxTreeMaskVarlenBatch = 1024;  // requests of a varlen mask build
+cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* kv_indptr, const int32_t* qo_indptr, int batch,
+                             int T, uint8_t* mask, int64_t mask_bytes, int32_t* mask_indptr, int64_t max_bytes,
+                             cudaStream_t stream);
 cudaError_t launch_relocate(void* pool, const int32_t* kv_indptr, int32_t* kv_indices, const int32_t* dst_start,
                             int batch, int64_t pool_rows, int64_t max_keys, uint32_t* status, cudaStream_t stream);
 int merge_blocks(int rows);

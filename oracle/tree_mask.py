@@ -10,12 +10,15 @@ prefix) or when draft node j - P_b is node i or an ancestor of i: a node of
 the tree sees itself and its ancestors [Capture Safety to MoE Ceiling,
 §"The Architecture of Capture Safety"; the tree semantics are the reading
 stated with the inputs].  A parent link outside [-1, node) ends the walk, as
-in the device builder's contract.
+in the device builder's contract.  In a varlen call request b has its own
+draft-token count T_b: its block is [T_b, P_b + T_b] and the offsets sum
+T_b * (P_b + T_b) (the uniform layout with q_len replaced by T_b).
 """
 
 from __future__ import annotations
 
-from typing import List, Sequence, Tuple
+import numbers
+from typing import List, Sequence, Tuple, Union
 
 
 def sees(parent: Sequence[int], i: int, d: int) -> bool:
@@ -29,15 +32,27 @@ def sees(parent: Sequence[int], i: int, d: int) -> bool:
     return False
 
 
-def mask_bits(parents: Sequence[Sequence[int]], prefix_lens: Sequence[int], T: int) -> Tuple[List[int], List[int]]:
-    """Flat list of bits of all requests' blocks and the bit offset of each block."""
+def _counts(T: Union[int, Sequence[int]], n: int) -> List[int]:
+    """Draft-token count of each request: one q_len for all, or one per request."""
+    return [int(T)] * n if isinstance(T, numbers.Integral) else [int(t) for t in T]
+
+
+def mask_bits(parents: Sequence[Sequence[int]], prefix_lens: Sequence[int],
+              T: Union[int, Sequence[int]]) -> Tuple[List[int], List[int]]:
+    """Flat list of bits of all requests' blocks and the bit offset of each block.
+
+    T is the q_len of every request, or a list of per-request counts T_b (a
+    varlen call): request b's block is then [T_b, P_b + T_b].
+    """
+    counts = _counts(T, len(prefix_lens))
     bits: List[int] = []
     offsets: List[int] = []
     for b, P in enumerate(prefix_lens):
         offsets.append(len(bits))
         par = parents[b]
-        for i in range(T):
-            for j in range(P + T):
+        Tb = counts[b]
+        for i in range(Tb):
+            for j in range(P + Tb):
                 if j < P:
                     bits.append(1)
                 else:
@@ -54,8 +69,9 @@ def pack_lsb(bits: Sequence[int]) -> List[int]:
     return out
 
 
-def build(parents: Sequence[Sequence[int]], prefix_lens: Sequence[int], T: int) -> Tuple[List[int], List[int]]:
-    """(packed mask bytes, mask_indptr) of a verify call."""
+def build(parents: Sequence[Sequence[int]], prefix_lens: Sequence[int],
+          T: Union[int, Sequence[int]]) -> Tuple[List[int], List[int]]:
+    """(packed mask bytes, mask_indptr) of a verify call (T: q_len, or per-request counts)."""
     bits, offsets = mask_bits(parents, prefix_lens, T)
     return pack_lsb(bits), offsets
 

@@ -159,3 +159,56 @@ def test_builder_and_verify_in_one_graph():
         o_ref, lse_ref = ref.verify(wl, nthreads=os.cpu_count() or 4)
         compare(bf16_to_f64(v.o[: 2 * T]).reshape(-1, 512), v.lse[: 2 * T].cpu().numpy().reshape(-1), o_ref,
                 lse_ref, "graph replay")
+
+
+# ---- varlen calls: per-request draft-token counts ---------------------------
+def _gpu_build_varlen(plan, parents, prefix_lens, Ts, fill=0xA5):
+    batch = len(prefix_lens)
+    indptr = np.concatenate([[0], np.cumsum(prefix_lens)]).astype(np.int32)
+    qo = np.concatenate([[0], np.cumsum(Ts)]).astype(np.int32)
+    flat = np.concatenate([np.asarray(p, np.int32) for p in parents] + [np.zeros(1, np.int32)])
+    total_bytes = (int(sum(t * (p + t) for p, t in zip(prefix_lens, Ts))) + 7) // 8
+    mask = torch.full((total_bytes + 64,), fill, dtype=torch.uint8, device="cuda")
+    mip = torch.full((max(batch, 1),), -7, dtype=torch.int32, device="cuda")
+    B.mla_verify_build_tree_mask_varlen(plan, torch.from_numpy(flat).cuda(), torch.from_numpy(indptr).cuda(),
+                                        torch.from_numpy(qo).cuda(), batch, mask, mip, mask_bytes=total_bytes)
+    torch.cuda.synchronize()
+    return mask.cpu().numpy(), mip.cpu().numpy()[:batch], total_bytes
+
+
+@pytest.mark.parametrize("seed,Ts,prefix", [
+    (0, [3, 0, 9, 1], [500, 40, 0, 1300]),
+    (1, [16, 1, 7], [257, 2000, 3]),
+    (2, [1] * 12, [int(x) for x in np.random.default_rng(2).integers(0, 400, 12)]),
+    (3, [9, 9], [100, 0]),
+    (4, [0, 0, 5], [10, 20, 30]),
+])
+def test_varlen_builder_matches_oracle_bit_for_bit(seed, Ts, prefix):
+    rng = np.random.default_rng(seed)
+    parents = [W.random_tree(rng, t) if t else np.zeros(0, np.int32) for t in Ts]
+    plan = _plan(len(Ts), max(Ts), max(p + t for p, t in zip(prefix, Ts)) + 1)
+    got, mip, n = _gpu_build_varlen(plan, parents, prefix, Ts)
+    ref, offs = TM.build([list(p) for p in parents], prefix, Ts)
+    assert got[:n].tolist() == ref
+    assert mip.tolist() == offs
+    assert (got[n:] == 0xA5).all(), "bytes past the mask were written"
+
+
+def test_varlen_verify_with_device_built_mask_is_identical():
+    wl = W.varlen_workload(B=4, H=64, T_list=[9, 0, 3, 1], prefix_lens=[800, 50, 2100, 0], pool_rows=8192, seed=5,
+                           nsplit=8)
+    v = B.verifier_for(wl)
+    d = B.device_inputs(wl)
+    o0, l0 = v.run(d, wl["B"], wl["sm_scale"])
+    o0, l0 = o0.clone(), l0.clone()
+    parents = torch.from_numpy(np.concatenate([np.asarray(p, np.int32) for p in wl["parents"]])).cuda()
+    mask = torch.zeros_like(d["custom_mask"])
+    mip = torch.zeros_like(d["mask_indptr"])
+    B.mla_verify_build_tree_mask_varlen(v.plan, parents, d["kv_indptr"], d["qo_indptr"], wl["B"], mask, mip)
+    torch.cuda.synchronize()
+    n = (int(sum(t * (p + t) for p, t in zip(wl["prefix_lens"], wl["T_list"]))) + 7) // 8
+    assert torch.equal(mask[:n], d["custom_mask"][:n]) and torch.equal(mip, d["mask_indptr"])
+    o1, l1 = v.run(dict(d, custom_mask=mask, mask_indptr=mip), wl["B"], wl["sm_scale"])
+    torch.cuda.synchronize()
+    rows = int(wl["qo_indptr"][-1])
+    assert torch.equal(o0[:rows].view(torch.int16), o1[:rows].view(torch.int16)) and torch.equal(l0[:rows], l1[:rows])

@@ -137,3 +137,44 @@ def _star_via_build(T, P):
     expect[:, 0] = 1
     expect[np.arange(T), np.arange(T)] = 1
     assert m[:, :P].all() and np.array_equal(m[:, P:], expect)
+
+
+# ---- varlen calls: per-request draft-token counts T_b ----------------------
+def test_varlen_equal_counts_equal_uniform():
+    rng = np.random.default_rng(12)
+    parents = [list(W.random_tree(rng, 6)) for _ in range(3)]
+    assert TM.build(parents, [5, 0, 9], [6, 6, 6]) == TM.build(parents, [5, 0, 9], 6)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_varlen_blocks_are_the_single_request_masks(seed):
+    """Request b's block is the one-request mask of (parents_b, P_b, T_b) at
+    bit offset sum_{b'<b} T_b' (P_b' + T_b'); a request with T_b = 0 has none."""
+    rng = np.random.default_rng(seed)
+    B = 5
+    Ts = [int(t) for t in rng.integers(0, 10, size=B)]
+    Ts[1] = 0
+    P = [int(p) for p in rng.integers(0, 40, size=B)]
+    parents = [list(W.random_tree(rng, t)) if t else [] for t in Ts]
+    bits, offsets = TM.mask_bits(parents, P, Ts)
+    acc = 0
+    for b in range(B):
+        assert offsets[b] == acc
+        alone, _ = TM.mask_bits([parents[b]], [P[b]], Ts[b])
+        assert bits[acc:acc + len(alone)] == alone
+        acc += Ts[b] * (P[b] + Ts[b])
+    assert len(bits) == acc
+
+
+@pytest.mark.parametrize("seed", [6, 7])
+def test_varlen_oracle_mask_with_brute_force_attention(oracle_lib, seed):
+    """Attention with the oracle's varlen mask (C oracle, reads bits) equals brute
+    force that takes visibility from the parent arrays."""
+    from oracle import brute
+    wl = W.varlen_workload(B=3, H=2, T_list=[4, 0, 7], prefix_lens=[6, 3, 11], pool_rows=256, seed=seed)
+    packed, offsets = TM.build([list(p) for p in wl["parents"]], list(wl["prefix_lens"]), list(wl["T_list"]))
+    wl = dict(wl, custom_mask=np.array(packed, np.uint8), mask_indptr=np.array(offsets, np.int32))
+    o, lse = oracle_lib.verify(wl, nthreads=2)
+    ob, lb = brute.brute_verify(wl)
+    np.testing.assert_allclose(o, np.array(ob), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, np.array(lb), rtol=0, atol=1e-12)
