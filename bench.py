@@ -95,13 +95,18 @@ def _strip_comments(src: str) -> str:
     return " ".join("".join(out).split())
 
 
+# The split kernel's sources: its instantiations and the headers they include.
+SPLIT_KERNEL_SOURCES = ("split_tc", "common.cuh", "tc_ptx.cuh", "merge_row.cuh")
+
+
 def kernel_source_hash(cdir: str = None) -> str:
-    """Hash of the kernel sources' code (comments and layout ignored): the ncu
-    counters in profiles/ stay valid across comment-only edits."""
+    """Hash of the split kernel's code (comments and layout ignored): the ncu
+    counters in profiles/ stay valid across comment-only edits and across
+    changes to the library's other kernels."""
     h = hashlib.sha256()
     cdir = cdir or os.path.join(ROOT, "mla_speculative_decode_tree_gb300", "csrc")
     for name in sorted(os.listdir(cdir)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith((".cu", ".cuh")) and name.startswith(SPLIT_KERNEL_SOURCES):
             with open(os.path.join(cdir, name), encoding="utf-8") as f:
                 h.update(name.encode() + _strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
