@@ -54,6 +54,26 @@ def test_noalloc_matches_workspace_call_twice_in_a_row():
         compare(a_o, a_l, r_o, r_l, "noalloc vs workspace, prefix=%s" % list(wl["prefix_lens"]))
 
 
+def test_noalloc_with_fused_merge_plan():
+    """A fused-merge plan on the scratch array: its arrival counters are zeroed
+    with the header each call; the results equal the plain plan's, bit for bit,
+    over three calls in a row."""
+    plain = B.Verifier(2, 64, 9, 3009, 16384, 8)
+    fused = B.mla_verify_plan(2, 64, 9, 3009, 16384, 8, B.MLA_VERIFY_FUSED_MERGE)
+    assert fused.describe().merge_blocks == 0 and fused.workspace_bytes <= SCRATCH_BYTES
+    o_na = torch.empty_like(plain.o)
+    lse_na = torch.empty_like(plain.lse)
+    for k, P in enumerate(([3000, 700], [129, 2500], [1, 3000])):
+        wl = W.tiny_workload(B=2, H=64, T=9, prefix_lens=P, pool_rows=16384, seed=50 + k, nsplit=8)
+        d = B.device_inputs(wl)
+        o_ref, lse_ref = plain.run(d, 2, wl["sm_scale"])
+        B.mla_verify_run_noalloc(fused, d["q_nope"], d["q_rope"], d["kv_pool"], d["kv_indptr"], d["kv_indices"],
+                                 d["out_cache_loc"], d["custom_mask"], d["mask_indptr"], 2, wl["sm_scale"], 8,
+                                 o_na, lse_na)
+        torch.cuda.synchronize()
+        assert torch.equal(o_na.view(torch.int16), o_ref.view(torch.int16)) and torch.equal(lse_na, lse_ref)
+
+
 def test_noalloc_rejects_plans_beyond_the_scratch_size():
     p = B.mla_verify_plan(1, 64, 9, 100000, 1 << 20, 64)  # 64 splits x 576 rows of partials > 32 MiB
     assert p.workspace_bytes > SCRATCH_BYTES
