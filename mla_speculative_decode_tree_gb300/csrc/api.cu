@@ -42,7 +42,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // counts per-key-step tensor time, which is bound by shared-memory operand
 // traffic (a fixed 4 KB key operand plus 32 bytes per query row):
 // ceil(rows/NQ) * (128 + NQ).
-const int kNqChoices[] = {16, 32, 48, 64, 80, 96};
+const int kNqChoices[] = {16, 32, 48, 64, 96};
 
 int pick_nq(int rows) {
   int best = 96;
@@ -94,7 +94,6 @@ int tc_smem(int nq) {
     case 32: return split_tc_smem_32();
     case 48: return split_tc_smem_48();
     case 64: return split_tc_smem_64();
-    case 80: return split_tc_smem_80();
     default: return split_tc_smem_96();
   }
 }
@@ -105,7 +104,6 @@ cudaError_t tc_launch(int nq, const SplitArgs& a, const TcMaps& m, dim3 grid, cu
     case 32: return launch_split_tc_32(a, m, grid, st);
     case 48: return launch_split_tc_48(a, m, grid, st);
     case 64: return launch_split_tc_64(a, m, grid, st);
-    case 80: return launch_split_tc_80(a, m, grid, st);
     default: return launch_split_tc_96(a, m, grid, st);
   }
 }

@@ -229,7 +229,6 @@ MLAV_DECLARE_TC(16)
 MLAV_DECLARE_TC(32)
 MLAV_DECLARE_TC(48)
 MLAV_DECLARE_TC(64)
-MLAV_DECLARE_TC(80)
 MLAV_DECLARE_TC(96)
 #undef MLAV_DECLARE_TC
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);

@@ -24,7 +24,7 @@
 // tile are fetched a second time (after the next tile's key blocks) rather
 // than kept resident: a whole 128-key tile (144 KB) does not fit next to Q.
 //
-// Warp roles (448 or 512 threads; CG = 3 column groups for NQ = 96, else 2):
+// Warp roles (512 threads; CG = 3 column groups for NQ = 96, else 2):
 //   warps 0..4CG-1  softmax.  Warp w reads TMEM lane quadrant w%4 (keys
 //              32(w%4)..+31 of the tile) and owns query columns
 //              [(w/4)*NQ/CG, (w/4+1)*NQ/CG).  It loads its scores once (the S^T
@@ -76,7 +76,7 @@ struct TcCfg {
   static constexpr int kPRegion = NQ * 128;  // P^T keys 0..63 or 64..127
   static constexpr int kPBytes = 2 * kPRegion;
   static constexpr int kSlotBytes = 128 * 128;
-  static constexpr int kStages = NQ >= 96 ? 5 : NQ >= 80 ? 6 : NQ >= 64 ? 8 : NQ >= 48 ? 9 : NQ >= 32 ? 11 : 12;
+  static constexpr int kStages = NQ >= 96 ? 5 : NQ >= 64 ? 8 : NQ >= 48 ? 9 : NQ >= 32 ? 11 : 12;
   static constexpr int kOffP = kQBytes;
   static constexpr int kOffRing = kQBytes + kPBytes;
   static constexpr int kOffCtl = kOffRing + kStages * kSlotBytes;

@@ -113,7 +113,7 @@ def test_plan_null_pointers(lib):
     (64, 9, 65545, 16, 0, 1, 64),  # 16 splits: 96 CTAs -> 9 x 16 = 144 fit one wave (48 rows: 192)
     (64, 9, 5009, 16, 0, 1, 64),   # 14 splits: 84 CTAs -> 9 x 14 = 126 (48 rows: 168)
     (64, 9, 4105, 16, 0, 1, 48),   # 11 splits: 66 CTAs -> 12 x 11 = 132
-    (8, 9, 5009, 16, 0, 1, 48),    # 72 rows: 1 group of 80 -> 2 groups of 48 (28 CTAs)
+    (8, 9, 5009, 16, 0, 1, 48),    # 72 rows: 1 group of 96 -> 2 groups of 48 (28 CTAs)
     (16, 4, 5004, 16, 0, 1, 48),   # 64 rows -> 48 + 16
     (8, 1, 5001, 16, 0, 0, 8),     # decode with 8 heads: tile mostly padding -> CUDA cores
     (64, 9, 5009, 16, B.MLA_VERIFY_FORCE_SIMT, 0, 8),

@@ -65,7 +65,7 @@ def test_parity_small_configs(name, flags):
 ADHOC = [
     # B, H, T, prefixes, pool, nsplit, tree
     (3, 64, 9, [0, 127, 1000], 4096, 4, "random"),   # empty prefix, ragged tail, multi-tile
-    (2, 8, 9, [128, 385], 2048, 3, "random"),        # H=8: 72 rows, one 80-row group
+    (2, 8, 9, [128, 385], 2048, 3, "random"),        # H=8: 72 rows, small grid -> 48-row groups
     (2, 16, 4, [256, 255], 2048, 2, "chain"),        # 64 rows
     (1, 64, 1, [700], 2048, 2, "random"),            # decode (T=1) on the tensor cores
     (2, 8, 1, [300, 5], 2048, 2, "random"),          # decode with 8 rows: CUDA-core path
@@ -77,7 +77,7 @@ ADHOC = [
     # moves small grids to 48 rows, so the others need grids of >= 152 CTAs)
     (2, 8, 4, [300, 77], 2048, 2, "random"),          # 32 rows -> 32-row groups
     (3, 16, 4, [2000, 300, 4000], 8192, 64, "random"),  # 64 rows, 192 CTAs -> 64-row groups
-    (4, 8, 9, [3000, 100, 5000, 64], 16384, 64, "random"),  # 72 rows, 160 CTAs -> 80-row groups
+    (4, 8, 9, [3000, 100, 5000, 64], 16384, 64, "random"),  # 72 rows, 256 CTAs -> one 96-row group
     (2, 64, 9, [5000, 3000], 16384, 64, "random"),    # 576 rows, 480 CTAs -> 96-row groups
     (1, 2, 64, [500], 4096, 2, "random"),             # q_len 64 (the maximum): 24 tokens per group
 ]
@@ -97,7 +97,7 @@ def test_every_row_group_size_is_exercised():
     for B_, H, T, prefixes, pool, nsplit, tree in ADHOC:
         L = max(prefixes) + T
         sizes.add(B.mla_verify_plan(B_, H, T, L, pool, nsplit).describe().rows_per_cta)
-    assert {16, 32, 48, 64, 80, 96} <= sizes, sizes
+    assert {16, 32, 48, 64, 96} <= sizes, sizes
 
 
 FULL = ["short4k", "mid64k", "long185k_h8", "batch16_ragged", "needle64k"]
