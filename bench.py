@@ -563,7 +563,8 @@ def run_gpu(args):
     }
     if rank == 0 and not args.no_sweep:
         sweep = {}
-        for name in ("mid64k", "mid64k_sorted", "long185k_h8", "batch16_ragged", "decode_b16", "varlen_b16"):
+        for name in ("mid64k", "mid64k_sorted", "long185k_h8", "batch16_ragged", "decode_b16", "decode_h8_b16",
+                     "varlen_b16"):
             try:
                 res = measure_workload(torch, name, min(args.steps, 30), 3, flush, stream)
                 s = summarize(res, peaks)

@@ -80,7 +80,7 @@ extern "C" {
  * merge_blocks = 0).  Results are bit-identical to the separate merge.  The
  * workspace gains one counter per (request, row group) between the header
  * and the partials; mla_verify_split is refused (EINVAL) for such a plan.
- * Ignored when the plan picks the CUDA-core kernel. */
+ * Ignored with MLA_VERIFY_FORCE_SIMT (the CUDA-core kernel keeps the separate merge). */
 #define MLA_VERIFY_FUSED_MERGE 0x2
 /* Test only: the tensor-core split kernel's gather never signals its first
  * block, so every CTA's bounded pipeline waits run out (about 2 s), the CTAs

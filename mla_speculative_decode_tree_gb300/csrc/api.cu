@@ -214,9 +214,12 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
   if (!pl) return MLA_VERIFY_EINVAL;
   pl->p = p;
   pl->rows_max = rows_max;
-  // Tensor cores unless the request's query rows would leave the smallest
-  // tile (16 columns) at least half padding.
-  pl->kernel = ((p.flags & MLA_VERIFY_FORCE_SIMT) || rows_b <= 8) ? 0 : 1;
+  // Tensor cores for every shape unless MLA_VERIFY_FORCE_SIMT.  Even where
+  // the 16-column tile is mostly padding (1 to 8 query rows) the kernel is
+  // bound by gathering the rows, not by the MMAs, and measured 6-8x faster
+  // than the CUDA-core kernel (16 requests x 8 heads x 1 token over 1k-33k
+  // keys: 146 against 1064 us per call).
+  pl->kernel = (p.flags & MLA_VERIFY_FORCE_SIMT) ? 0 : 1;
   pl->nq = pl->kernel ? choose_nq(rows_b, p.max_kv_len, p.nsplit, p.max_batch) : kSimtRowsPerCta;
   pl->groups = (int)((rows_b + pl->nq - 1) / pl->nq);
   pl->smem = pl->kernel ? tc_smem(pl->nq) : 0;

@@ -1,9 +1,10 @@
 // CUDA-core split kernel: one warp per query row (token, head), warp-shuffle
 // dot products and an online softmax over the keys of one split.
 //
-// This is the shape-agnostic path: it serves shapes whose query rows per
-// request would leave the tensor-core tile mostly padding, and it is the
-// independent second implementation the tensor-core kernel is compared with.
+// This is the shape-agnostic path, taken with MLA_VERIFY_FORCE_SIMT: the
+// independent second implementation the tensor-core kernel is compared with
+// (the planner uses the tensor cores for every shape, also for one to eight
+// query rows per request, where this kernel measured 6-8x slower).
 // Each lane owns 16 of the 512 latent columns (16-byte chunks l and l+32 of a
 // row) and lanes 0-7 also own one 16-byte chunk of the 64 RoPE columns, so a
 // key row is fetched with 128-bit loads [Capture Safety to MoE Ceiling,

@@ -207,6 +207,9 @@ CONFIGS = {
     # T = 1 decode on the verify kernels, and per-request draft-token counts
     "decode_b16": VerifyConfig("decode_b16", B=16, H=64, T=1, prefix=(1024, 32768), pool_rows=1048576,
                                nsplit=16),
+    # decode on one tensor-parallel shard (8 heads): the CUDA-core kernel's shape
+    "decode_h8_b16": VerifyConfig("decode_h8_b16", B=16, H=8, T=1, prefix=(1024, 32768), pool_rows=1048576,
+                                  nsplit=16),
     "varlen_b16": VerifyConfig("varlen_b16", B=16, H=64, T=16, prefix=(1024, 32768), pool_rows=1048576,
                                nsplit=16, T_range=(1, 16)),
 }

@@ -66,9 +66,9 @@ def test_fused_merge_plan(lib):
     off_lse = (256 + 4 * 2 * info.grid_x + 255) // 256 * 256
     off_o = (off_lse + 4 * 16 * rows + 255) // 256 * 256
     assert p.workspace_bytes == off_o + 4 * 16 * rows * 512
-    simt = plan(num_heads=2, q_len=4, flags=B.MLA_VERIFY_FUSED_MERGE)
+    simt = plan(num_heads=2, q_len=4, flags=B.MLA_VERIFY_FUSED_MERGE | B.MLA_VERIFY_FORCE_SIMT)
     assert simt.describe().kernel == 0 and simt.describe().merge_blocks > 0
-    assert simt.workspace_bytes == plan(num_heads=2, q_len=4).workspace_bytes
+    assert simt.workspace_bytes == plan(num_heads=2, q_len=4, flags=B.MLA_VERIFY_FORCE_SIMT).workspace_bytes
     ptr = FAKE
     rc = lib.mla_verify_split(ctypes.c_void_p(p.handle), ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 1, 0.072, 16, FAKE,
                               p.workspace_bytes, None)
@@ -115,7 +115,7 @@ def test_plan_null_pointers(lib):
     (64, 9, 4105, 16, 0, 1, 48),   # 11 splits: 66 CTAs -> 12 x 11 = 132
     (8, 9, 5009, 16, 0, 1, 48),    # 72 rows: 1 group of 96 -> 2 groups of 48 (28 CTAs)
     (16, 4, 5004, 16, 0, 1, 48),   # 64 rows -> 48 + 16
-    (8, 1, 5001, 16, 0, 0, 8),     # decode with 8 heads: tile mostly padding -> CUDA cores
+    (8, 1, 5001, 16, 0, 1, 16),    # decode with 8 heads: 16-row tile, half padding, still tensor cores
     (64, 9, 5009, 16, B.MLA_VERIFY_FORCE_SIMT, 0, 8),
 ])
 def test_plan_kernel_choice(lib, H, T, kv, ns, flags, kernel, nq):

@@ -68,7 +68,7 @@ ADHOC = [
     (2, 8, 9, [128, 385], 2048, 3, "random"),        # H=8: 72 rows, small grid -> 48-row groups
     (2, 16, 4, [256, 255], 2048, 2, "chain"),        # 64 rows
     (1, 64, 1, [700], 2048, 2, "random"),            # decode (T=1) on the tensor cores
-    (2, 8, 1, [300, 5], 2048, 2, "random"),          # decode with 8 rows: CUDA-core path
+    (2, 8, 1, [300, 5], 2048, 2, "random"),          # decode with 8 rows: half-empty 16-row tile
     (2, 5, 7, [200, 333], 2048, 3, "random"),        # 35 rows -> 48-row group, tokens straddle groups
     (1, 1, 16, [90], 1024, 1, "random"),             # 16 rows, one head
     (1, 32, 3, [5000], 8192, 64, "random"),          # more splits than needed: empty splits
