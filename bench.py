@@ -241,14 +241,14 @@ def capture(torch, fn, stream):
     return g
 
 
-def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False, flags=0):
+def measure_workload(torch, name, steps, warmup, flush, stream, with_e2e=False, flags=0, nsplit=None):
     from mla_speculative_decode_tree_gb300 import binding as B
     from mla_speculative_decode_tree_gb300 import workloads as W
 
     cfg = W.CONFIGS[name]
     wl = W.make_workload(cfg)
     d = B.device_inputs(wl)
-    v = B.verifier_for(wl, flags=flags)
+    v = B.verifier_for(wl, flags=flags, nsplit=nsplit)
     info = v.plan.describe()
     scale = wl["sm_scale"]
 
@@ -575,6 +575,22 @@ def run_gpu(args):
                 sweep[name] = {"error": repr(exc)[:200]}
             torch.cuda.empty_cache()
         line["sweep"] = sweep
+        auto = {}
+        for name in ("short4k", "mid64k", "long185k_h8", "batch16_ragged", "decode_b16"):
+            try:
+                res = measure_workload(torch, name, min(args.steps, 30), 3, flush, stream, nsplit=0)
+                s = summarize(res, peaks)
+                auto[name] = {"us_per_call": round(s["us_per_call"], 3), "split_us": round(s["split_us"], 3),
+                              "roofline_frac": round(s["roofline_frac"], 4), "rows_per_cta": s["rows_per_cta"],
+                              "chunks_per_request": res["info"].grid_y,
+                              "nsplit_given_us_per_call": (round(us_call, 3) if name == args.workload else
+                                                           sweep.get(name, {}).get("us_per_call")),
+                              "status": res["status"]}
+                del res
+            except Exception as exc:
+                auto[name] = {"error": repr(exc)[:200]}
+            torch.cuda.empty_cache()
+        line["auto_split"] = auto
         fused = {}
         for name in ("short4k", "mid64k", "decode_b16"):
             try:

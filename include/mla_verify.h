@@ -96,7 +96,11 @@ typedef struct {
   int32_t q_len;      /* T in [1, 64]: draft tokens per request (uniform) */
   int32_t max_kv_len; /* >= max_b (P_b + T); documents the longest request (chunk size is per request) */
   int64_t pool_rows;  /* rows in kv_pool; keys resolving outside [0, pool_rows) are left out and flagged */
-  int32_t nsplit;     /* >= 1: KV chunks per request = partials per output row (fixed grid dimension) */
+  int32_t nsplit;     /* >= 1: KV chunks per request (chunk = ceil(L_b/nsplit) rounded up to 128 keys)
+                       *       = partials per output row (fixed grid dimension);
+                       * 0: the plan picks the number of chunks (describe().grid_y) and the
+                       *    row-group size for this GPU from max_batch and max_kv_len; runs then
+                       *    pass nsplit = 0 as well */
   int32_t d_latent;   /* must be 512 */
   int32_t d_rope;     /* must be 64 */
   int32_t flags;      /* OR of MLA_VERIFY_FORCE_SIMT, MLA_VERIFY_FUSED_MERGE, MLA_VERIFY_TEST_STALL_GATHER */

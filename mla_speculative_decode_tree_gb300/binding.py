@@ -314,4 +314,5 @@ class Verifier:
 
 def verifier_for(wl: dict, flags: int = 0, nsplit: Optional[int] = None, device="cuda") -> Verifier:
     L = int(max(wl["prefix_lens"])) + wl["T"] if len(wl["prefix_lens"]) else wl["T"]  # bounds P_b + T_b too
-    return Verifier(wl["B"], wl["H"], wl["T"], L, wl["pool"].shape[0], nsplit or wl["nsplit"], flags, device)
+    return Verifier(wl["B"], wl["H"], wl["T"], L, wl["pool"].shape[0], wl["nsplit"] if nsplit is None else nsplit,
+                    flags, device)

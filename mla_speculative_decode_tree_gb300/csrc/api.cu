@@ -21,6 +21,7 @@ struct mla_verify_plan_s {
   int groups;  // row groups per request
   int64_t rows_max;
   bool fused;  // the split kernel merges (MLA_VERIFY_FUSED_MERGE on the tensor-core kernel)
+  int splits;  // KV chunks per request = grid dimension = partials per row (nsplit, or the plan's count)
   size_t off_cnt, off_lse, off_o, ws_bytes;  // [0, off_lse) must be zero between calls
   int merge_blocks;
   int smem;
@@ -86,6 +87,51 @@ int choose_nq(int64_t rows_b, int64_t max_kv_len, int nsplit, int max_batch) {
   for (int nq : kNqChoices)
     if (nq >= 48 && nq <= base && ctas(nq) <= sms) return nq;
   return base;
+}
+
+// nsplit = 0: the plan picks the row-group size and the number of KV
+// chunks per request (chunks stay ceil(L_b/nsplit) rounded up to 128 keys).
+// Cost model, from measurements on GB300: a CTA is bound by landing its
+// gathered blocks, ~6.5 us per 128-key tile (17 blocks of 16 KB at ~0.38 us)
+// whatever its row-group size, plus ~6 us of start-up and epilogue; the
+// merge reads each written partial (2 KB per row) at ~3 TB/s after a ~2 us
+// launch.  One request: CTAs of equal length run in waves of one per SM.
+// Several requests (lengths unknown at plan time, taken as half of
+// max_kv_len on average): the CTAs are list-scheduled, so the time is about
+// the work per SM plus one chunk of the longest request.
+struct SplitChoice {
+  int nq, splits;
+};
+SplitChoice choose_auto_split(int64_t rows_b, int64_t max_kv_len, int max_batch, bool tensor_cores) {
+  constexpr double kTileUs = 6.5, kCtaUs = 6.0, kMergeUs = 2.0, kMergeBytesPerUs = 3.0e6;
+  const double sms = (double)device_sm_count();
+  const int64_t tiles_max = (max_kv_len + kKeysPerTile - 1) / kKeysPerTile;
+  SplitChoice best{tensor_cores ? 96 : kSimtRowsPerCta, 1};
+  double best_t = -1.0;
+  for (int nq : kNqChoices) {
+    if (!tensor_cores && nq != kNqChoices[0]) break;
+    const int rows_per = tensor_cores ? nq : kSimtRowsPerCta;
+    const double groups = (double)((rows_b + rows_per - 1) / rows_per);
+    for (int64_t n = 1; n <= tiles_max && n <= 4096; ++n) {
+      const int64_t per = (tiles_max + n - 1) / n;  // tiles in a chunk of the longest request
+      if (n > 1 && (tiles_max + n - 2) / (n - 1) == per) continue;  // same chunks, more partials
+      double t;
+      if (max_batch == 1) {
+        const double waves = std::ceil(groups * n / sms);
+        t = waves * (per * kTileUs + kCtaUs) + kMergeUs + n * rows_b * 2048.0 / kMergeBytesPerUs;
+      } else {
+        const double work = groups * max_batch * tiles_max / 2.0;  // tiles, all CTAs
+        const double ctas = groups * max_batch * n;
+        t = (work / sms + per) * kTileUs + ctas * kCtaUs / sms + kMergeUs +
+            (double)n * rows_b * max_batch * 2048.0 / kMergeBytesPerUs;
+      }
+      if (best_t < 0 || t < best_t) {
+        best_t = t;
+        best = {rows_per, (int)n};
+      }
+    }
+  }
+  return best;
 }
 
 int tc_smem(int nq) {
@@ -200,7 +246,7 @@ extern "C" {
 int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, mla_verify_plan_t* out) {
   if (!params || !workspace_bytes || !out) return MLA_VERIFY_EINVAL;
   const mla_verify_params& p = *params;
-  if (p.max_batch < 1 || p.num_heads < 1 || p.q_len < 1 || p.q_len > kMaxQLen || p.nsplit < 1 ||
+  if (p.max_batch < 1 || p.num_heads < 1 || p.q_len < 1 || p.q_len > kMaxQLen || p.nsplit < 0 ||
       p.pool_rows < 1 || p.max_kv_len < p.q_len)
     return MLA_VERIFY_EINVAL;
   if (p.d_latent != kDLatent || p.d_rope != kDRope) return MLA_VERIFY_EUNSUPPORTED;
@@ -220,7 +266,14 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
   // than the CUDA-core kernel (16 requests x 8 heads x 1 token over 1k-33k
   // keys: 146 against 1064 us per call).
   pl->kernel = (p.flags & MLA_VERIFY_FORCE_SIMT) ? 0 : 1;
-  pl->nq = pl->kernel ? choose_nq(rows_b, p.max_kv_len, p.nsplit, p.max_batch) : kSimtRowsPerCta;
+  if (p.nsplit == 0) {
+    const SplitChoice c = choose_auto_split(rows_b, p.max_kv_len, p.max_batch, pl->kernel == 1);
+    pl->nq = c.nq;
+    pl->splits = c.splits;
+  } else {
+    pl->nq = pl->kernel ? choose_nq(rows_b, p.max_kv_len, p.nsplit, p.max_batch) : kSimtRowsPerCta;
+    pl->splits = p.nsplit;
+  }
   pl->groups = (int)((rows_b + pl->nq - 1) / pl->nq);
   pl->smem = pl->kernel ? tc_smem(pl->nq) : 0;
 
@@ -228,8 +281,8 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
   pl->off_cnt = kWsHeader;
   pl->off_lse = pl->fused ? round_up(pl->off_cnt + sizeof(uint32_t) * (size_t)p.max_batch * pl->groups, 256)
                           : kWsHeader;
-  pl->off_o = round_up(pl->off_lse + sizeof(float) * (size_t)p.nsplit * (size_t)rows_max, 256);
-  pl->ws_bytes = pl->off_o + sizeof(float) * (size_t)p.nsplit * (size_t)rows_max * kDLatent;
+  pl->off_o = round_up(pl->off_lse + sizeof(float) * (size_t)pl->splits * (size_t)rows_max, 256);
+  pl->ws_bytes = pl->off_o + sizeof(float) * (size_t)pl->splits * (size_t)rows_max * kDLatent;
   pl->merge_blocks = pl->fused ? 0 : merge_blocks((int)rows_max);
   *workspace_bytes = pl->ws_bytes;
   *out = pl;
@@ -242,7 +295,7 @@ int mla_verify_plan_describe(mla_verify_plan_t pl, mla_verify_plan_info* info) {
   info->rows_per_cta = pl->nq;
   info->keys_per_tile = kKeysPerTile;
   info->grid_x = pl->groups;
-  info->grid_y = pl->p.nsplit;
+  info->grid_y = pl->splits;
   info->grid_z = pl->p.max_batch;
   info->merge_blocks = pl->merge_blocks;
   info->smem_bytes = pl->smem;
@@ -286,7 +339,7 @@ int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_
   a.batch = batch;
   a.H = pl->p.num_heads;
   a.T = pl->p.q_len;
-  a.nsplit = pl->p.nsplit;
+  a.nsplit = pl->splits;
   a.pool_rows = pl->p.pool_rows;
   a.rows_max = pl->rows_max;
   a.scale_log2 = sm_scale * 1.4426950408889634f;
@@ -298,7 +351,7 @@ int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_
   a.o = pl->fused ? static_cast<__nv_bfloat16*>(o) : nullptr;
   a.lse = pl->fused ? lse : nullptr;
 
-  const dim3 grid(pl->groups, pl->p.nsplit, pl->p.max_batch);
+  const dim3 grid(pl->groups, pl->splits, pl->p.max_batch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (pl->kernel) {
@@ -331,7 +384,7 @@ int merge_impl(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, const int32_
   m.qo_indptr = qo_indptr;
   m.batch = batch;
   m.H = pl->p.num_heads;
-  m.nsplit = pl->p.nsplit;
+  m.nsplit = pl->splits;
   m.rows_max = pl->rows_max;
   m.part_lse = reinterpret_cast<const float*>(ws + pl->off_lse);
   m.part_o = reinterpret_cast<const float*>(ws + pl->off_o);

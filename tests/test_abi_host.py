@@ -86,7 +86,7 @@ def test_plan_accepts_the_test_stall_flag(lib):
     (dict(q_len=65), B.MLA_VERIFY_EINVAL),
     (dict(num_heads=0), B.MLA_VERIFY_EINVAL),
     (dict(max_batch=0), B.MLA_VERIFY_EINVAL),
-    (dict(nsplit=0), B.MLA_VERIFY_EINVAL),
+    (dict(nsplit=-1), B.MLA_VERIFY_EINVAL),
     (dict(pool_rows=0), B.MLA_VERIFY_EINVAL),
     (dict(max_kv_len=3), B.MLA_VERIFY_EINVAL),
     (dict(flags=0x200), B.MLA_VERIFY_EINVAL),
@@ -174,3 +174,18 @@ def test_relocate_host_validation(lib):
     assert call(ws_bytes=p.workspace_bytes - 1) == B.MLA_VERIFY_EWORKSPACE
     assert call(ws=FAKE + 16) == B.MLA_VERIFY_EINVAL        # workspace not 256-byte aligned
     assert lib.mla_verify_relocate_kv(None, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1 << 30, None) == B.MLA_VERIFY_EINVAL
+
+
+def test_auto_split_plan(lib):
+    """nsplit = 0: the plan picks the number of chunks per request (the grid's
+    split dimension) and sizes the workspace by it."""
+    p = plan(max_batch=1, max_kv_len=65545, pool_rows=1 << 20, nsplit=0)
+    info = p.describe()
+    assert info.kernel == 1 and 1 <= info.grid_y <= 513  # at most one chunk per 128-key tile
+    rows = 9 * 64
+    off_o = (256 + 4 * info.grid_y * rows + 255) // 256 * 256
+    assert p.workspace_bytes == off_o + 4 * info.grid_y * rows * 512
+    assert plan(nsplit=16).describe().grid_y == 16
+    # the run's nsplit must be the plan's (0)
+    assert run_raw(lib, p, nsplit=16) == B.MLA_VERIFY_EINVAL
+    assert run_raw(lib, p, nsplit=0, batch=0) == B.MLA_VERIFY_OK

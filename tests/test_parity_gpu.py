@@ -265,3 +265,35 @@ def test_split_and_merge_entry_points_match_run():
     B.mla_verify_merge(v.plan, 1, 4, v.workspace, o2, l2)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2[:9]) and torch.equal(l1, l2[:9])
+
+
+# ---- nsplit = 0: the number of chunks chosen by the plan --------------------
+AUTO_SPLIT = [
+    # B, H, T, prefixes, pool
+    (1, 64, 9, [4096], 16384),
+    (3, 64, 9, [0, 127, 3000], 8192),      # ragged, an empty prefix
+    (1, 8, 9, [20000], 32768),             # few rows: long chunks, one row group
+    (2, 16, 1, [5000, 77], 8192),          # decode
+    (1, 2, 64, [900], 4096),               # q_len 64
+]
+
+
+@pytest.mark.parametrize("flags", [0, B.MLA_VERIFY_FORCE_SIMT], ids=["auto", "simt"])
+@pytest.mark.parametrize("case", AUTO_SPLIT, ids=[str(i) for i in range(len(AUTO_SPLIT))])
+def test_parity_auto_split(case, flags):
+    Bn, H, T, prefixes, pool = case
+    wl = W.tiny_workload(B=Bn, H=H, T=T, prefix_lens=prefixes, pool_rows=pool, seed=sum(prefixes) + 3 * H, nsplit=4)
+    _, v = check_full(wl, flags, nsplit=0, what="nsplit=0 " + str(case))
+    assert v.plan.nsplit == 0 and v.plan.describe().grid_y >= 1
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["short4k", "long185k_h8"])
+def test_auto_split_full_size_sampled(name):
+    from oracle import ref
+    wl = W.make_workload(W.CONFIGS[name])
+    o, lse, st, v = gpu_run(wl, nsplit=0)
+    assert st == 0
+    rows = sample_rows(wl, per_request=8)
+    o_ref, lse_ref = ref.verify(wl, rows=rows, nthreads=NTHREADS)
+    compare(o[rows], lse[rows], o_ref, lse_ref, name + " nsplit=0")
