@@ -112,6 +112,11 @@ def kernel_source_hash(cdir: str = None) -> str:
     return h.hexdigest()[:16]
 
 
+def traffic_key(workload: str, nsplit=None) -> str:
+    """Key of a stored traffic record: the workload, with the nsplit override if any."""
+    return workload if nsplit is None else "%s@nsplit%d" % (workload, nsplit)
+
+
 def ncu_traffic(workload: str):
     """DRAM bytes per split-kernel launch from the committed ncu summary, if it matches this source."""
     path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
@@ -471,7 +476,7 @@ def run_gpu(args):
     cfg = W.CONFIGS[args.workload]
     wl = W.make_workload(cfg)
     d = B.device_inputs(wl)
-    v = B.verifier_for(wl)
+    v = B.verifier_for(wl, nsplit=args.nsplit)
     info = v.plan.describe()
 
     def call():
@@ -532,7 +537,7 @@ def run_gpu(args):
         achieved = alg["split_bytes"] / (split_us * 1e-6) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
     roofline = {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(traffic_key(args.workload, args.nsplit)),
                 "kernel": "split (%s, %d query rows/CTA)" % ("tcgen05" if info.kernel else "cuda-core",
                                                               info.rows_per_cta),
                 "peak_source": "%s (burst: kernel timed alone)" % peak_src,
@@ -542,7 +547,9 @@ def run_gpu(args):
         "metric": METRIC, "value": round(us_call, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "l2": "flushed (512 MiB write) before every step",
+        "config": {"workload": workload_desc(cfg) + ("" if args.nsplit is None else
+                                                      " (run with nsplit=%d: %d chunks)" % (args.nsplit, info.grid_y)),
+                   "l2": "flushed (512 MiB write) before every step",
                    "parallelism": "replicas" if world > 1 else "single GPU", "graph": "split+merge in one CUDA graph"},
         "us_per_call_median": round(float(np.median(step_ms)) * 1e3, 3),
         "us_per_call_p10_p90": [round(float(np.percentile(step_ms, 10)) * 1e3, 3),
@@ -745,11 +752,13 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="store the split kernel's DRAM bytes per launch from an ncu CSV for --workload, then exit")
+    ap.add_argument("--nsplit", type=int, default=None,
+                    help="run the headline workload with this nsplit instead of its own (0: the plan picks)")
     ap.add_argument("--relocation-only", action="store_true",
                     help="time only the KV relocation call on --workload's rows (steps/warmup as given)")
     args = ap.parse_args(argv)
     if args.record_traffic:
-        print(json.dumps(record_traffic(args.record_traffic, args.workload)))
+        print(json.dumps(record_traffic(args.record_traffic, traffic_key(args.workload, args.nsplit))))
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
