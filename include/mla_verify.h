@@ -28,7 +28,8 @@
  * O = 0 and LSE = -inf.
  *
  * The computation is split-K: each request's key range is cut into `nsplit`
- * chunks, one CTA per (chunk, group of query rows, request) writes a partial
+ * chunks (or as many as the plan picked, nsplit = 0), one CTA per (chunk,
+ * group of query rows, request) writes a partial
  * (normalised O, LSE) into the workspace, and a second kernel merges the
  * partials by log-sum-exp [Custom sm_120 Verify Kernel, §"Building the
  * Custom Kernel: From Occupancy Starvation to Flash-Decode"].  The grid is
@@ -111,7 +112,7 @@ typedef struct {
   int32_t kernel;        /* 1 = tcgen05 tensor-core split kernel, 0 = CUDA-core split kernel */
   int32_t rows_per_cta;  /* query rows (token x head pairs) one split CTA covers */
   int32_t keys_per_tile; /* keys per pipeline tile (chunk sizes are multiples of it) */
-  int32_t grid_x, grid_y, grid_z; /* split grid: row groups x nsplit x max_batch */
+  int32_t grid_x, grid_y, grid_z; /* split grid: row groups x KV chunks per request x max_batch */
   int32_t merge_blocks;  /* merge grid size; 0 when the split kernel merges (MLA_VERIFY_FUSED_MERGE) */
   int32_t smem_bytes;    /* dynamic shared memory of the split kernel */
   size_t workspace_bytes;
@@ -121,7 +122,8 @@ typedef struct {
  * Validate `params` and build a plan.  Host only: touches no device state.
  * On success *out receives the plan and *workspace_bytes the size of the
  * device workspace every run with this plan needs (fp32 partial O and LSE
- * for nsplit x max_batch*q_len*num_heads rows plus a 256-byte header, and
+ * for grid_y x max_batch*q_len*num_heads rows -- grid_y = nsplit, or the
+ * plan's count when nsplit = 0 -- plus a 256-byte header, and
  * for MLA_VERIFY_FUSED_MERGE one 32-bit counter per request and row group).
  * The workspace must be 256-byte aligned and zero-filled once before its
  * first use (e.g. torch.zeros, or mla_verify_workspace_init); the library
@@ -151,7 +153,7 @@ int mla_verify_plan_describe(mla_verify_plan_t plan, mla_verify_plan_info* info)
  *  mask_indptr      int32 [batch] bit offsets (B entries, not B+1)
  *  batch            0 <= batch <= max_batch (0 enqueues nothing)
  *  sm_scale         score scale (1/sqrt(192) for the K2-class MLA geometry)
- *  nsplit           must equal the plan's nsplit
+ *  nsplit           must equal the plan's nsplit (0 for a plan that picked its own count)
  *  workspace        device buffer of >= the plan's workspace_bytes (see mla_verify_plan)
  *  o                bf16 [batch*q_len, num_heads, 512] output (round-to-nearest-even)
  *  lse              fp32 [batch*q_len, num_heads] output, natural log
