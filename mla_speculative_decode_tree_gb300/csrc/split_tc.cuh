@@ -378,11 +378,17 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
       bool ok = mbar_wait_spin(&ctl.q_full, 0, &ctl.abort, a.status);
       // cp.async writes shared memory through the generic proxy and the MMA
       // reads it through the async proxy: a proxy fence follows each acquire.
-      auto take = [&](int& slot) -> bool {
+      auto wait_full = [&](int& slot) -> bool {
         slot = seq % S;
-        const bool r = mbar_wait_spin(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
+        return mbar_wait_spin(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
+      };
+      auto fences = [&]() {
         fence_proxy_async_smem();
         tc::fence_after_sync();
+      };
+      auto take = [&](int& slot) -> bool {
+        const bool r = wait_full(slot);
+        fences();
         return r;
       };
       // A slot is free again once the MMAs reading it are done.
@@ -420,15 +426,17 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
 #pragma unroll 1
           for (int m = 0; m < 4 && ok; ++m) {
             int sa, sb;
-            if (seq % S == S - 1) {
-              if (!(ok = take(sa))) break;
+            if (seq % S == S - 1) {  // filler slot: nothing to read
+              if (!(ok = wait_full(sa))) break;
               release(sa);
               ++seq;
             }
-            if (!(ok = take(sa))) break;
+            // one fence after both halves of the pair have landed
+            if (!(ok = wait_full(sa))) break;
             ++seq;
-            if (!(ok = take(sb))) break;
+            if (!(ok = wait_full(sb))) break;
             ++seq;
+            fences();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint64_t adesc =
