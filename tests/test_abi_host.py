@@ -189,3 +189,16 @@ def test_auto_split_plan(lib):
     # the run's nsplit must be the plan's (0)
     assert run_raw(lib, p, nsplit=16) == B.MLA_VERIFY_EINVAL
     assert run_raw(lib, p, nsplit=0, batch=0) == B.MLA_VERIFY_OK
+
+
+@pytest.mark.parametrize("B_,H,T,kv,nq,splits", [
+    (1, 64, 9, 4105, 96, 17),     # short4k: one wave of 102 CTAs, 2 tiles each
+    (1, 64, 9, 65545, 96, 25),    # mid64k: one wave of 150 CTAs
+    (1, 8, 9, 185009, 96, 145),   # long185k_h8: one row group, 145 CTAs of 10 tiles
+])
+def test_auto_split_choices_on_152_sms(lib, B_, H, T, kv, nq, splits):
+    """The cost model's picks for single requests on a 152-SM GB300 (the host
+    fallback count when no device answers)."""
+    info = plan(max_batch=B_, num_heads=H, q_len=T, max_kv_len=kv, pool_rows=1 << 20, nsplit=0).describe()
+    assert (info.rows_per_cta, info.grid_y) == (nq, splits)
+    assert -(-H * T // nq) * splits * B_ <= 152
