@@ -87,3 +87,20 @@ def test_planted_mistakes_fail_a_pin(bug):
         == list(range(int(wl["dst_start"][b]), int(wl["dst_start"][b]) + int(wl["prefix_lens"][b])))
         for b in range(wl["B"]))
     assert not (same_result and contiguous)
+
+
+def test_free_block_workload_keeps_destinations_free():
+    """The relocation inputs: every row the call addresses lies outside the
+    destination blocks, and those blocks do not overlap."""
+    wl = W.with_free_block(W.tiny_workload(B=4, H=2, T=3, prefix_lens=[50, 0, 17, 200], pool_rows=1024, seed=2),
+                           seed=3)
+    addressed = set(W.logical_rows(wl).tolist())
+    blocks = []
+    for b in range(wl["B"]):
+        start, n = int(wl["dst_start"][b]), int(wl["prefix_lens"][b])
+        blocks.append(set(range(start, start + n)))
+    assert all(not (blk & addressed) for blk in blocks)
+    for i in range(len(blocks)):
+        for j in range(i + 1, len(blocks)):
+            assert not (blocks[i] & blocks[j])
+    assert all(0 <= r < wl["pool_rows"] for blk in blocks for r in blk)
