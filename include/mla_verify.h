@@ -83,6 +83,13 @@ extern "C" {
  * and the partials; mla_verify_split is refused (EINVAL) for such a plan.
  * Ignored with MLA_VERIFY_FORCE_SIMT (the CUDA-core kernel keeps the separate merge). */
 #define MLA_VERIFY_FUSED_MERGE 0x2
+/* Run the tensor-core split kernel in its value-refetch mode: each 128-key
+ * tile's 8 value blocks are gathered a second time for the PV product, which
+ * allows row groups of up to 96 query rows.  Without this flag the kernel
+ * keeps each tile resident in shared memory (row groups of at most 64 rows,
+ * each key gathered once per row group).  Results agree within rounding;
+ * the flag exists to compare the two modes. */
+#define MLA_VERIFY_REFETCH_VALUES 0x4
 /* Test only: the tensor-core split kernel's gather never signals its first
  * block, so every CTA's bounded pipeline waits run out (about 2 s), the CTAs
  * drain and return, and the call reports MLA_VERIFY_DEV_TIMEOUT; its outputs
@@ -104,7 +111,8 @@ typedef struct {
                        *    pass nsplit = 0 as well */
   int32_t d_latent;   /* must be 512 */
   int32_t d_rope;     /* must be 64 */
-  int32_t flags;      /* OR of MLA_VERIFY_FORCE_SIMT, MLA_VERIFY_FUSED_MERGE, MLA_VERIFY_TEST_STALL_GATHER */
+  int32_t flags;      /* OR of MLA_VERIFY_FORCE_SIMT, MLA_VERIFY_FUSED_MERGE, MLA_VERIFY_REFETCH_VALUES,
+                       * MLA_VERIFY_TEST_STALL_GATHER */
 } mla_verify_params;
 
 /* What a plan chose (for tests, benchmarks and logs). */
@@ -116,6 +124,8 @@ typedef struct {
   int32_t merge_blocks;  /* merge grid size; 0 when the split kernel merges (MLA_VERIFY_FUSED_MERGE) */
   int32_t smem_bytes;    /* dynamic shared memory of the split kernel */
   size_t workspace_bytes;
+  int32_t resident_tile; /* 1: tensor-core kernel keeps each key tile resident (one gather per key and
+                          * row group); 0: value blocks gathered twice, or the CUDA-core kernel */
 } mla_verify_plan_info;
 
 /*

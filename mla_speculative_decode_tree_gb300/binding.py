@@ -24,6 +24,7 @@ MLA_VERIFY_DEV_BAD_ROW = 0x1
 MLA_VERIFY_DEV_TIMEOUT = 0x2
 MLA_VERIFY_FORCE_SIMT = 0x1
 MLA_VERIFY_FUSED_MERGE = 0x2
+MLA_VERIFY_REFETCH_VALUES = 0x4
 MLA_VERIFY_TEST_STALL_GATHER = 0x100
 
 EXPORTED = ("mla_verify_plan", "mla_verify_plan_describe", "mla_verify_run", "mla_verify_split",
@@ -42,7 +43,7 @@ class MlaVerifyPlanInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32), ("keys_per_tile", ctypes.c_int32),
                 ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),
                 ("merge_blocks", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("resident_tile", ctypes.c_int32)]
 
 
 class MlaVerifyError(RuntimeError):

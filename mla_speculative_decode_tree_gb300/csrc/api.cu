@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -18,6 +19,7 @@ struct mla_verify_plan_s {
   mla_verify_params p;
   int kernel;  // 1 = tcgen05, 0 = CUDA cores
   int nq;      // query rows per split CTA
+  bool resident;  // tensor-core kernel in resident-tile mode (each key lands once per CTA)
   int groups;  // row groups per request
   int64_t rows_max;
   bool fused;  // the split kernel merges (MLA_VERIFY_FUSED_MERGE on the tensor-core kernel)
@@ -39,24 +41,9 @@ int cuda_fail(cudaError_t e) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Candidate row-group sizes of the tensor-core kernel.  The cost model
-// counts per-key-step tensor time, which is bound by shared-memory operand
-// traffic (a fixed 4 KB key operand plus 32 bytes per query row):
-// ceil(rows/NQ) * (128 + NQ).
+// Row-group sizes of the tensor-core kernel (resident mode: at most 64).
 const int kNqChoices[] = {16, 32, 48, 64, 96};
-
-int pick_nq(int rows) {
-  int best = 96;
-  long best_cost = -1;
-  for (int nq : kNqChoices) {
-    const long cost = (long)((rows + nq - 1) / nq) * (128 + nq);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = nq;
-    }
-  }
-  return best;
-}
+constexpr int kMaxResidentNq = 64;
 
 // SMs of the current device (152 on GB300, also when no device can be asked).
 int device_sm_count() {
@@ -69,88 +56,100 @@ int device_sm_count() {
   return n;
 }
 
-// Rows per CTA.  pick_nq() minimises the tensor work; but when that grid is a
-// single partial wave (short prefixes, few heads), smaller row groups put more
-// CTAs on the idle SMs and each CTA, with less of Q and P^T in shared memory,
-// keeps more gathered blocks in flight: then take the smallest size, not below
-// 48 rows, whose grid still fits in one wave (measured on GB300: a 4k prefix
-// with 64 heads x 9 tokens went from 34.9 to 31.4 us, a 185k prefix with 8
-// heads from 172 to 162 us; a 64k prefix, three waves at 96 rows, is not
-// affected).
-int choose_nq(int64_t rows_b, int64_t max_kv_len, int nsplit, int max_batch) {
-  const int base = pick_nq((int)rows_b);
+// Time model of a split launch, from measurements on GB300 (clocks at
+// 2070 MHz).  A CTA is bound by landing its gathered blocks, not by its MMAs:
+// a 128-key tile takes ~5.1 us when it stays resident (one landing per key,
+// but each tile waits out its own landing), and ~5.3-5.9 us when the value
+// blocks are fetched a second time through the ring (17 blocks at ~0.34 us;
+// larger row groups leave fewer ring slots beside Q).  A CTA adds ~5 us of
+// start-up, first landing and epilogue; the merge reads each written partial
+// (2 KB per row) at ~3 TB/s after a ~2 us launch.  One request: CTAs of equal
+// length run in waves of one per SM.  Several requests (lengths unknown at
+// plan time, taken as half of max_kv_len on average): the CTAs are
+// list-scheduled, so the time is about the work per SM plus one chunk of the
+// longest request.
+double tile_us(bool resident, int nq) { return resident ? 5.1 : nq >= 96 ? 5.9 : nq >= 64 ? 5.6 : 5.3; }
+
+double est_us(int64_t rows_b, int64_t max_kv_len, int max_batch, int nsplit, int nq, bool resident, double sms) {
+  constexpr double kCtaUs = 5.0, kMergeUs = 2.0, kMergeBytesPerUs = 3.0e6;
+  const double groups = (double)((rows_b + nq - 1) / nq);
   const int64_t chunk = chunk_len(max_kv_len, nsplit);
-  const int64_t splits = (max_kv_len + chunk - 1) / chunk;  // non-empty splits of the longest request
-  const int64_t sms = device_sm_count();
-  auto ctas = [&](int nq) { return (rows_b + nq - 1) / nq * splits * max_batch; };
-  if (ctas(base) >= sms) return base;
-  for (int nq : kNqChoices)
-    if (nq >= 48 && nq <= base && ctas(nq) <= sms) return nq;
-  return base;
+  const double per = (double)(chunk / kKeysPerTile);                 // tiles in a chunk of the longest request
+  const double splits = (double)((max_kv_len + chunk - 1) / chunk);  // its non-empty chunks
+  const double tiles_max = (double)((max_kv_len + kKeysPerTile - 1) / kKeysPerTile);
+  const double tu = tile_us(resident, nq);
+  double t;
+  if (max_batch == 1) {
+    t = std::ceil(groups * splits / sms) * (per * tu + kCtaUs);
+  } else {
+    const double work = groups * max_batch * tiles_max / 2.0;
+    t = (work / sms + per) * tu + groups * max_batch * splits * kCtaUs / sms;
+  }
+  return t + kMergeUs + splits * rows_b * max_batch * 2048.0 / kMergeBytesPerUs;
 }
 
-// nsplit = 0: the plan picks the row-group size and the number of KV
-// chunks per request (chunks stay ceil(L_b/nsplit) rounded up to 128 keys).
-// Cost model, from measurements on GB300: a CTA is bound by landing its
-// gathered blocks, ~6.5 us per 128-key tile (17 blocks of 16 KB at ~0.38 us)
-// whatever its row-group size, plus ~6 us of start-up and epilogue; the
-// merge reads each written partial (2 KB per row) at ~3 TB/s after a ~2 us
-// launch.  One request: CTAs of equal length run in waves of one per SM.
-// Several requests (lengths unknown at plan time, taken as half of
-// max_kv_len on average): the CTAs are list-scheduled, so the time is about
-// the work per SM plus one chunk of the longest request.
-struct SplitChoice {
+// Mode and row-group size for a given split count (and, nsplit = 0, the
+// split count too): the least modelled time; among choices within 2 % of it,
+// the least per-key cost ceil(rows/NQ) * (128 + NQ) -- each row group lands
+// every key and reads its 4 KB key operand per k-step, each query row adds
+// 32 bytes of operand -- then the fewest splits (fewest partials), then the
+// resident mode.
+struct Choice {
+  bool resident;
   int nq, splits;
 };
-SplitChoice choose_auto_split(int64_t rows_b, int64_t max_kv_len, int max_batch, bool tensor_cores) {
-  constexpr double kTileUs = 6.5, kCtaUs = 6.0, kMergeUs = 2.0, kMergeBytesPerUs = 3.0e6;
+Choice choose(int64_t rows_b, int64_t max_kv_len, int max_batch, int nsplit, bool allow_resident) {
   const double sms = (double)device_sm_count();
   const int64_t tiles_max = (max_kv_len + kKeysPerTile - 1) / kKeysPerTile;
-  SplitChoice best{tensor_cores ? 96 : kSimtRowsPerCta, 1};
-  double best_t = -1.0;
-  for (int nq : kNqChoices) {
-    if (!tensor_cores && nq != kNqChoices[0]) break;
-    const int rows_per = tensor_cores ? nq : kSimtRowsPerCta;
-    const double groups = (double)((rows_b + rows_per - 1) / rows_per);
-    for (int64_t n = 1; n <= tiles_max && n <= 4096; ++n) {
-      const int64_t per = (tiles_max + n - 1) / n;  // tiles in a chunk of the longest request
-      if (n > 1 && (tiles_max + n - 2) / (n - 1) == per) continue;  // same chunks, more partials
-      double t;
-      if (max_batch == 1) {
-        const double waves = std::ceil(groups * n / sms);
-        t = waves * (per * kTileUs + kCtaUs) + kMergeUs + n * rows_b * 2048.0 / kMergeBytesPerUs;
-      } else {
-        const double work = groups * max_batch * tiles_max / 2.0;  // tiles, all CTAs
-        const double ctas = groups * max_batch * n;
-        t = (work / sms + per) * kTileUs + ctas * kCtaUs / sms + kMergeUs +
-            (double)n * rows_b * max_batch * 2048.0 / kMergeBytesPerUs;
+  const int64_t n_lo = nsplit > 0 ? nsplit : 1;
+  const int64_t n_hi = nsplit > 0 ? nsplit : std::min<int64_t>(tiles_max, 4096);
+  auto for_each = [&](auto&& fn) {
+    for (int res = allow_resident ? 1 : 0; res >= 0; --res)  // resident first: it wins exact ties
+      for (int nq : kNqChoices) {
+        if (res && nq > kMaxResidentNq) continue;
+        for (int64_t n = n_lo; n <= n_hi; ++n) {
+          if (nsplit == 0 && n > 1 && (tiles_max + n - 2) / (n - 1) == (tiles_max + n - 1) / n)
+            continue;  // same chunks as n - 1 splits, only more partials
+          fn(res != 0, nq, (int)n, est_us(rows_b, max_kv_len, max_batch, (int)n, nq, res != 0, sms));
+        }
       }
-      if (best_t < 0 || t < best_t) {
-        best_t = t;
-        best = {rows_per, (int)n};
-      }
+  };
+  double t_min = -1.0;
+  for_each([&](bool, int, int, double t) {
+    if (t_min < 0 || t < t_min) t_min = t;
+  });
+  Choice best{false, 96, (int)n_lo};
+  int64_t best_work = -1;
+  int best_n = 0;
+  for_each([&](bool res, int nq, int n, double t) {
+    if (t > t_min * 1.02) return;
+    const int64_t work = (rows_b + nq - 1) / nq * (128 + nq);
+    if (best_work < 0 || work < best_work || (work == best_work && n < best_n)) {
+      best_work = work;
+      best_n = n;
+      best = {res, nq, n};
     }
-  }
+  });
   return best;
 }
 
-int tc_smem(int nq) {
+int tc_smem(int nq, bool res) {
   switch (nq) {
-    case 16: return split_tc_smem_16();
-    case 32: return split_tc_smem_32();
-    case 48: return split_tc_smem_48();
-    case 64: return split_tc_smem_64();
-    default: return split_tc_smem_96();
+    case 16: return split_tc_smem_16(res);
+    case 32: return split_tc_smem_32(res);
+    case 48: return split_tc_smem_48(res);
+    case 64: return split_tc_smem_64(res);
+    default: return split_tc_smem_96(res);
   }
 }
 
-cudaError_t tc_launch(int nq, const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t st) {
+cudaError_t tc_launch(int nq, bool res, const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t st) {
   switch (nq) {
-    case 16: return launch_split_tc_16(a, m, grid, st);
-    case 32: return launch_split_tc_32(a, m, grid, st);
-    case 48: return launch_split_tc_48(a, m, grid, st);
-    case 64: return launch_split_tc_64(a, m, grid, st);
-    default: return launch_split_tc_96(a, m, grid, st);
+    case 16: return launch_split_tc_16(a, m, grid, st, res);
+    case 32: return launch_split_tc_32(a, m, grid, st, res);
+    case 48: return launch_split_tc_48(a, m, grid, st, res);
+    case 64: return launch_split_tc_64(a, m, grid, st, res);
+    default: return launch_split_tc_96(a, m, grid, st, res);
   }
 }
 
@@ -250,7 +249,8 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
       p.pool_rows < 1 || p.max_kv_len < p.q_len)
     return MLA_VERIFY_EINVAL;
   if (p.d_latent != kDLatent || p.d_rope != kDRope) return MLA_VERIFY_EUNSUPPORTED;
-  if ((p.flags & ~(MLA_VERIFY_FORCE_SIMT | MLA_VERIFY_FUSED_MERGE | MLA_VERIFY_TEST_STALL_GATHER)) != 0)
+  if ((p.flags & ~(MLA_VERIFY_FORCE_SIMT | MLA_VERIFY_FUSED_MERGE | MLA_VERIFY_REFETCH_VALUES |
+                   MLA_VERIFY_TEST_STALL_GATHER)) != 0)
     return MLA_VERIFY_EINVAL;
   const int64_t rows_b = (int64_t)p.q_len * p.num_heads;
   const int64_t rows_max = rows_b * p.max_batch;
@@ -266,16 +266,25 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
   // than the CUDA-core kernel (16 requests x 8 heads x 1 token over 1k-33k
   // keys: 146 against 1064 us per call).
   pl->kernel = (p.flags & MLA_VERIFY_FORCE_SIMT) ? 0 : 1;
-  if (p.nsplit == 0) {
-    const SplitChoice c = choose_auto_split(rows_b, p.max_kv_len, p.max_batch, pl->kernel == 1);
+  if (pl->kernel) {
+    // The mode (resident tile, unless MLA_VERIFY_REFETCH_VALUES), the row-group
+    // size and, for nsplit = 0, the split count, from the time model.
+    const Choice c = choose(rows_b, p.max_kv_len, p.max_batch, p.nsplit, !(p.flags & MLA_VERIFY_REFETCH_VALUES));
+    pl->resident = c.resident;
     pl->nq = c.nq;
     pl->splits = c.splits;
   } else {
-    pl->nq = pl->kernel ? choose_nq(rows_b, p.max_kv_len, p.nsplit, p.max_batch) : kSimtRowsPerCta;
-    pl->splits = p.nsplit;
+    // CUDA-core kernel (8 query rows per CTA); nsplit = 0 aims at about four
+    // CTAs per SM in all.
+    pl->resident = false;
+    pl->nq = kSimtRowsPerCta;
+    const int64_t rows = ((rows_b + kSimtRowsPerCta - 1) / kSimtRowsPerCta) * p.max_batch;
+    const int64_t tiles = (p.max_kv_len + kKeysPerTile - 1) / kKeysPerTile;
+    const int64_t want = std::max<int64_t>(1, (int64_t)device_sm_count() * 4 / std::max<int64_t>(rows, 1));
+    pl->splits = p.nsplit > 0 ? p.nsplit : (int)std::min<int64_t>(want, tiles);
   }
   pl->groups = (int)((rows_b + pl->nq - 1) / pl->nq);
-  pl->smem = pl->kernel ? tc_smem(pl->nq) : 0;
+  pl->smem = pl->kernel ? tc_smem(pl->nq, pl->resident) : 0;
 
   pl->fused = pl->kernel == 1 && (p.flags & MLA_VERIFY_FUSED_MERGE);
   pl->off_cnt = kWsHeader;
@@ -293,6 +302,7 @@ int mla_verify_plan_describe(mla_verify_plan_t pl, mla_verify_plan_info* info) {
   if (!pl || !info) return MLA_VERIFY_EINVAL;
   info->kernel = pl->kernel;
   info->rows_per_cta = pl->nq;
+  info->resident_tile = pl->resident ? 1 : 0;
   info->keys_per_tile = kKeysPerTile;
   info->grid_x = pl->groups;
   info->grid_y = pl->splits;
@@ -365,7 +375,7 @@ int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_
         (rc = encode_bf16_2d(enc, &maps.qn, q_nope_absorbed, kDLatent, rows_total, 64, pl->nq)) != MLA_VERIFY_OK ||
         (rc = encode_bf16_2d(enc, &maps.qr, q_rope, kDRope, rows_total, 64, pl->nq)) != MLA_VERIFY_OK)
       return rc;
-    e = tc_launch(pl->nq, a, maps, grid, st);
+    e = tc_launch(pl->nq, pl->resident, a, maps, grid, st);
   } else {
     e = launch_split_simt(a, grid, st);
   }

@@ -222,9 +222,11 @@ __device__ __forceinline__ uint32_t mask_bit(const uint8_t* mask, int64_t bit) {
 
 // Host launchers (defined in the kernel translation units).
 cudaError_t launch_split_simt(const SplitArgs& a, dim3 grid, cudaStream_t stream);
-#define MLAV_DECLARE_TC(NQ)                                                                         \
-  cudaError_t launch_split_tc_##NQ(const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t stream); \
-  int split_tc_smem_##NQ();
+// resident: whole-tile mode (NQ <= 64; the 96-row launcher refuses it).
+#define MLAV_DECLARE_TC(NQ)                                                                            \
+  cudaError_t launch_split_tc_##NQ(const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t stream, \
+                                   bool resident);                                                     \
+  int split_tc_smem_##NQ(bool resident);
 MLAV_DECLARE_TC(16)
 MLAV_DECLARE_TC(32)
 MLAV_DECLARE_TC(48)

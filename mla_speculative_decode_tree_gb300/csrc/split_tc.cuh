@@ -43,11 +43,26 @@
 //              or out_cache_loc (drafts, at the request's token rows)
 //              [Capture Safety to MoE Ceiling, §"The Architecture of Capture
 //              Safety"]; Q arrives once by 2-D TMA.
-// Block sequence through the ring: K(0), K(1), V(0), K(2), V(1), ...,
-// K(nt-1), V(nt-2), V(nt-1), where K(t) is the 9 column blocks of tile t and
-// V(t) its first 8 in pairs (one M=128 block of latent columns per pair).  A
-// pair must occupy adjacent slots, so an empty slot is inserted whenever a
-// pair would start in the last slot; producer and consumer apply the same rule.
+// Two ways to feed the tiles (kMode):
+//
+// kRefetch (up to 96 query rows).  Block sequence through the ring: K(0),
+// K(1), V(0), K(2), V(1), ..., K(nt-1), V(nt-2), V(nt-1), where K(t) is the
+// 9 column blocks of tile t and V(t) its first 8 in pairs (one M=128 block of
+// latent columns per pair).  A pair must occupy adjacent slots, so an empty
+// slot is inserted whenever a pair would start in the last slot; producer
+// and consumer apply the same rule.
+//
+// kResident (at most 64 query rows).  Q then takes at most 72 KB, so a whole
+// tile fits beside it: nine fixed slots, slot b holding column block b of the
+// current tile.  Each key lands once per CTA and feeds both products: QK(t)
+// reads all nine blocks; P^T(t) is written into slot 8 (the RoPE block,
+// which only QK reads) once QK(t) is complete; PV(t) reads slots 0..7 and
+// P^T, releasing the value pair (2m, 2m+1) after M-block m, and slot 8 last.
+// The gather refills each slot with the next tile's block as soon as it is
+// released.  The MMA thread issues QK(t), PV(t), QK(t+1), ..., so the commit
+// that completes S^T(t) also covers PV(t-1): the softmax may rescale O^T and
+// write P^T right after it, with no other wait.  The next tile's blocks land
+// only after PV(t), so every tile waits out one landing.
 //
 // Every wait is bounded (mbar_wait, mbar_wait_spin for the MMA thread); on a
 // timeout the CTA raises the status bit, all roles drain, the in-flight MMAs
@@ -62,9 +77,14 @@ namespace mlav {
 
 constexpr float kTau = 8.0f;  // base-2 headroom before the running max is raised
 
-template <int NQ>
+enum TcMode : int { kRefetch = 0, kResident = 1 };
+
+template <int NQ, int kMode>
 struct TcCfg {
   static_assert(NQ % 16 == 0 && NQ >= 16 && NQ <= 96, "NQ must be a multiple of 16 in [16, 96]");
+  static constexpr bool kLandOnce = kMode != kRefetch;  // each key lands once per CTA
+  static_assert(!kLandOnce || NQ <= 64, "resident tiles fit beside Q for at most 64 query rows");
+  static constexpr int kKeys = kKeysPerTile;  // keys per tile = M of the QK MMA
   static constexpr int kCG = NQ == 96 ? 3 : 2;  // softmax warps per TMEM lane quadrant
   static constexpr int kHC = NQ / kCG;          // query columns per softmax thread
   static constexpr int kSoftmaxWarps = 4 * kCG;
@@ -73,30 +93,39 @@ struct TcCfg {
   static_assert(kHC % 8 == 0, "columns per softmax thread must be a multiple of 8");
   static constexpr int kQBlock = NQ * 128;  // one 64-column block of Q
   static constexpr int kQBytes = 9 * kQBlock;
-  static constexpr int kPRegion = NQ * 128;  // P^T keys 0..63 or 64..127
-  static constexpr int kPBytes = 2 * kPRegion;
-  static constexpr int kSlotBytes = 128 * 128;
-  static constexpr int kStages = NQ >= 96 ? 5 : NQ >= 64 ? 8 : NQ >= 48 ? 9 : NQ >= 32 ? 11 : 12;
-  static constexpr int kOffP = kQBytes;
-  static constexpr int kOffRing = kQBytes + kPBytes;
+  static constexpr int kPRegion = NQ * 128;  // P^T for 64 keys (keys 0..63 or 64..127 of a tile)
+  static constexpr int kPBytes = (kKeys / 64) * kPRegion;
+  static constexpr int kSlotBytes = kKeys * 128;  // one 64-column block of a tile
+  static_assert(!kLandOnce || kPBytes <= kSlotBytes, "P^T must fit in the RoPE block's slot");
+  static constexpr int kStages =
+      kLandOnce ? 9 : NQ >= 96 ? 5 : NQ >= 64 ? 8 : NQ >= 48 ? 9 : NQ >= 32 ? 11 : 12;
+  static constexpr int kOffRing = kLandOnce ? kQBytes : kQBytes + kPBytes;
+  // P^T: its own buffer, or (resident) the RoPE block's slot 8
+  static constexpr int kOffP = kLandOnce ? kOffRing + 8 * kSlotBytes : kQBytes;
   static constexpr int kOffCtl = kOffRing + kStages * kSlotBytes;
   static constexpr int kOStride = (NQ + 31) / 32 * 32;  // TMEM columns per O^T block (32-aligned)
-  static constexpr int kColS = 4 * kOStride;
-  // Gather warps: up to 16 warps in all, and no more than ring slots.  A warp
-  // fills every kProducerWarps-th block; with more warps than slots it could
-  // reach a slot whose empty barrier is two phases behind, where the parity
-  // wait cannot tell the phases apart.
+  static constexpr int kColS = 4 * kOStride;            // S^T
+  static_assert(kColS + kOStride <= 512, "TMEM budget");
+  // Column sums: thread tid < 2*NQ sums half a row of P^T (64 keys) per
+  // tile.  In resident mode these warps release slot 8 together with the MMA.
+  static constexpr int kPSumWarps = 2 * NQ / 32;
+  // Gather warps: up to 16 warps in all.  kRefetch: no more than ring slots;
+  // a warp fills every kProducerWarps-th block, and with more warps than slots
+  // it could reach a slot whose empty barrier is two phases behind, where the
+  // parity wait cannot tell the phases apart.  kResident: warp w owns slots
+  // w, w + kProducerWarps, ... of every tile, so it always waits on a slot it
+  // filled itself one tile earlier.
   static constexpr int kProducerWarp = kSoftmaxWarps + 1;
   static constexpr int kProducerWarps = (15 - kSoftmaxWarps) < kStages ? (15 - kSoftmaxWarps) : kStages;
   static_assert(kProducerWarps >= 1 && kProducerWarps <= kStages, "gather warps must not outnumber ring slots");
   static constexpr int kThreads = 32 * (kProducerWarp + kProducerWarps);
 };
 
-template <int NQ>
+template <int NQ, int kMode>
 struct TcCtl {
-  uint64_t full[TcCfg<NQ>::kStages];
-  uint64_t empty[TcCfg<NQ>::kStages];
-  uint64_t q_full, s_full, s_free, p_full, pv_done[2], mma_idle;
+  uint64_t full[TcCfg<NQ, kMode>::kStages];
+  uint64_t empty[TcCfg<NQ, kMode>::kStages];
+  uint64_t q_full, s_full, s_free, p_full, pv_done[2], pv_last, mma_idle;
   uint32_t tmem_base;
   int abort;
   int merge_last;  // fused merge: this CTA is the last of its row group to finish
@@ -110,9 +139,9 @@ struct TcCtl {
   uint64_t colmask[kMaxQLen][3];  // per token: which of a column group's columns belong to it
 };
 
-template <int NQ>
+template <int NQ, int kMode>
 constexpr int tc_smem_bytes() {
-  return TcCfg<NQ>::kOffCtl + (int)sizeof(TcCtl<NQ>) + 1024;  // + alignment slack
+  return TcCfg<NQ, kMode>::kOffCtl + (int)sizeof(TcCtl<NQ, kMode>) + 1024;  // + alignment slack
 }
 
 // Bounded wait that ignores the abort flag (teardown only).
@@ -162,11 +191,15 @@ __device__ __forceinline__ void warp_columns_to_smem(const float (&x)[HC], float
 }
 
 // kFused: the CTA that finishes a row group last also merges it (a separate
-// instantiation, so the plain kernel carries none of that code).
-template <int NQ, bool kFused>
-__global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
+// instantiation, so the plain kernel carries none of that code).  kMode:
+// how the tiles are fed (see above).
+template <int NQ, bool kFused, int kMode>
+__global__ void __launch_bounds__(TcCfg<NQ, kMode>::kThreads, 1)
     split_tc_kernel(const __grid_constant__ SplitArgs a, const __grid_constant__ TcMaps maps) {
-  using Cfg = TcCfg<NQ>;
+  using Cfg = TcCfg<NQ, kMode>;
+  constexpr bool kLandOnce = Cfg::kLandOnce;
+  constexpr int kKeys = Cfg::kKeys;
+  constexpr int kM = kKeys / 32;  // row ids per gather lane and tile
   constexpr int S = Cfg::kStages;
   constexpr int HC = Cfg::kHC;
   constexpr int CG = Cfg::kCG;
@@ -200,7 +233,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     for (int n = tid; n < nrows; n += kTcThreads) lse_out[n] = -INFINITY;
     return;
   }
-  const int nt = (int)((j1 - j0 + kKeysPerTile - 1) / kKeysPerTile);
+  const int nt = (int)((j1 - j0 + kKeys - 1) / kKeys);
   const int i0 = r0 / a.H;
   const int ntok = (r0 + nrows - 1) / a.H - i0 + 1;
   // The row groups of a split read the same keys; group g starts g tiles
@@ -218,13 +251,15 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw_addr + pad;
   const uint32_t sQ = sbase, sP = sbase + Cfg::kOffP, sRing = sbase + Cfg::kOffRing;
-  TcCtl<NQ>& ctl = *reinterpret_cast<TcCtl<NQ>*>(smem + Cfg::kOffCtl);
+  TcCtl<NQ, kMode>& ctl = *reinterpret_cast<TcCtl<NQ, kMode>*>(smem + Cfg::kOffCtl);
 
   // ---- set-up ---------------------------------------------------------------
   if (tid == 0) {
     for (int k = 0; k < S; ++k) {
       mbar_init(&ctl.full[k], 32);  // every lane of the filling warp
-      mbar_init(&ctl.empty[k], 1);
+      // resident mode: slot 8 (P^T) is free once PV has read it and the
+      // column-sum warps are done with it
+      mbar_init(&ctl.empty[k], (kLandOnce && k == 8) ? 1 + Cfg::kPSumWarps : 1);
     }
     mbar_init(&ctl.q_full, 1);
     mbar_init(&ctl.s_full, 1);
@@ -232,6 +267,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     mbar_init(&ctl.p_full, kSoftmaxWarps);
     mbar_init(&ctl.pv_done[0], 1);
     mbar_init(&ctl.pv_done[1], 1);
+    mbar_init(&ctl.pv_last, 1);
     mbar_init(&ctl.mma_idle, 1);
     ctl.abort = 0;
     ctl.rflag[0] = ctl.rflag[1] = 0;
@@ -263,9 +299,10 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
 
   if (warp >= kProducerWarp) {
     // =========================== gather ======================================
-    // The gather warps walk the same block sequence and take turns: warp pw
-    // fills the blocks with seq % kProducerWarps == pw.  A block is 128 keys x
-    // 64 columns: lane (jl = lane/8, c = lane%8) copies 16-byte chunk c of
+    // Value-refetch mode: the gather warps walk the same block sequence and
+    // take turns, warp pw filling the blocks with seq % kProducerWarps == pw.
+    // Resident mode: warp pw owns fixed slots.  A block is 128 keys x 64
+    // columns: lane (jl = lane/8, c = lane%8) copies 16-byte chunk c of
     // keys 4*it + jl, it = 0..31, into its swizzled place (cp.async, L2 only);
     // the copies of a lane signal full[slot] when they land.
     const int pw = warp - kProducerWarp;
@@ -285,85 +322,115 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     // loaded while tile t is fetched), so no gather warp waits on an index
     // load between tiles.
     auto key_of = [&](int tile, int m) -> int64_t {
-      return j0 + (int64_t)tile * kKeysPerTile + 4 * (c8 + 8 * m) + jl;
+      return j0 + (int64_t)tile * kKeys + 4 * (c8 + 8 * m) + jl;
     };
-    auto load_ids = [&](int t, int (&raw)[4]) {
+    auto load_ids = [&](int t, int (&raw)[kM]) {
       const int tile = tile_at(t < nt ? t : 0);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
+      for (int m = 0; m < kM; ++m) {
         const int64_t j = key_of(tile, m);
         raw[m] = (t < nt && j < j1) ? load_row_id(a, rq.q0, P, kv_base, j) : -1;
       }
     };
     int64_t rsub = resolve_row(a, rq.q0, P, kv_base, j0);
-    int raw_cur[4], raw_nxt[4];
+    int raw_cur[kM], raw_nxt[kM];
     load_ids(0, raw_cur);
     load_ids(1, raw_nxt);
     if (rsub < 0) rsub = 0;
-    int own[4] = {0, 0, 0, 0}, prev[4] = {0, 0, 0, 0};
+    int own[kM], prev[kM];
+#pragma unroll
+    for (int m = 0; m < kM; ++m) own[m] = prev[m] = 0;
     uint32_t bad = 0;
-    int seq = 0;
-    bool stop = false;
-    auto produce = [&](int blk, const int (&r)[4]) {
-      if (stop) return;
-      if (seq % Cfg::kProducerWarps != pw) {
-        ++seq;
-        return;
-      }
-      const int slot = seq % S;
-      // every lane acquires the slot; the warp stops together if any gave up
-      const bool got = mbar_wait(&ctl.empty[slot], ((seq / S) & 1) ^ 1, &ctl.abort, a.status);
-      if (!__all_sync(0xffffffffu, got)) {
-        stop = true;
-        return;
-      }
-      if (a.test_stall && seq == 0) {
-        // test only: block 0 is never filled nor signalled
-      } else if (blk >= 0) {
-        const uint32_t base = sRing + slot * Cfg::kSlotBytes + jl * 128;
-        const __nv_bfloat16* src0 = a.kv_pool + blk * 64 + c8 * 8;
+    // Rows of tile t (tile_at(t)) into own[], the previous tile's into prev[];
+    // then the index loads of tile t+2 are issued.
+    auto next_rows = [&](int t) {
+      const int tile = tile_at(t);
 #pragma unroll
-        for (int it = 0; it < 32; ++it) {
-          const int row = __shfl_sync(0xffffffffu, r[it >> 3], 8 * jl + (it & 7));
-          const int swz = (c8 ^ (4 * (it & 1) + jl)) << 4;  // key (4*it + jl) mod 8 = 4*(it%2) + jl
-          cp_async16(base + it * 512 + swz, src0 + (int64_t)row * kDRow, 16u);
+      for (int m = 0; m < kM; ++m) {
+        prev[m] = own[m];
+        int64_t rr = rsub;
+        if (key_of(tile, m) < j1) {
+          if (raw_cur[m] >= 0 && raw_cur[m] < a.pool_rows)
+            rr = raw_cur[m];
+          else
+            bad = 1;
         }
-        cp_async_arrive(&ctl.full[slot]);
-      } else {
-        mbar_arrive(&ctl.full[slot]);
+        own[m] = (int)rr;
+        raw_cur[m] = raw_nxt[m];
       }
-      ++seq;
+      load_ids(t + 2, raw_nxt);
     };
-#pragma unroll 1
-    for (int t = 0; t <= nt && !stop; ++t) {
-      if (t < nt) {
-        const int tile = tile_at(t);
+    // Column block blk of the keys whose rows r[] holds, into `slot`; the
+    // copies of every lane signal full[slot] when they land.
+    auto copy_block = [&](int slot, int blk, const int (&r)[kM]) {
+      const uint32_t base = sRing + slot * Cfg::kSlotBytes + jl * 128;
+      const __nv_bfloat16* src0 = a.kv_pool + blk * 64 + c8 * 8;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          prev[m] = own[m];
-          int64_t rr = rsub;
-          if (key_of(tile, m) < j1) {
-            if (raw_cur[m] >= 0 && raw_cur[m] < a.pool_rows)
-              rr = raw_cur[m];
-            else
-              bad = 1;
-          }
-          own[m] = (int)rr;
-          raw_cur[m] = raw_nxt[m];
-        }
-        load_ids(t + 2, raw_nxt);
-#pragma unroll 1
-        for (int blk = 0; blk < 9; ++blk) produce(blk, own);
+      for (int it = 0; it < kKeys / 4; ++it) {
+        const int row = __shfl_sync(0xffffffffu, r[it >> 3], 8 * jl + (it & 7));
+        const int swz = (c8 ^ (4 * (it & 1) + jl)) << 4;  // key (4*it + jl) mod 8 = 4*(it%2) + jl
+        cp_async16(base + it * 512 + swz, src0 + (int64_t)row * kDRow, 16u);
       }
-      if (t >= 1) {
-        // value blocks of tile t-1: its rows are in prev[] (or still in own[]
-        // after the last tile)
-        const bool last = (t == nt);
+      cp_async_arrive(&ctl.full[slot]);
+    };
+    bool stop = false;
+    if constexpr (kLandOnce) {
+      // Warp pw fills slots pw, pw + kProducerWarps, ... of every tile, each
+      // once the previous tile has released it.
 #pragma unroll 1
-        for (int pr = 0; pr < 4; ++pr) {
-          if (seq % S == S - 1) produce(-1, own);
-          produce(2 * pr, last ? own : prev);
-          produce(2 * pr + 1, last ? own : prev);
+      for (int t = 0; t < nt && !stop; ++t) {
+        next_rows(t);
+#pragma unroll 1
+        for (int blk = pw; blk < 9; blk += Cfg::kProducerWarps) {
+          const bool got = mbar_wait(&ctl.empty[blk], (t & 1) ^ 1, &ctl.abort, a.status);
+          if (!__all_sync(0xffffffffu, got)) {
+            stop = true;
+            break;
+          }
+          if (!(a.test_stall && t == 0 && blk == 0)) copy_block(blk, blk, own);  // test only: block 0 never lands
+        }
+      }
+    } else {
+      int seq = 0;
+      auto produce = [&](int blk, const int (&r)[kM]) {
+        if (stop) return;
+        if (seq % Cfg::kProducerWarps != pw) {
+          ++seq;
+          return;
+        }
+        const int slot = seq % S;
+        // every lane acquires the slot; the warp stops together if any gave up
+        const bool got = mbar_wait(&ctl.empty[slot], ((seq / S) & 1) ^ 1, &ctl.abort, a.status);
+        if (!__all_sync(0xffffffffu, got)) {
+          stop = true;
+          return;
+        }
+        if (a.test_stall && seq == 0) {
+          // test only: block 0 is never filled nor signalled
+        } else if (blk >= 0) {
+          copy_block(slot, blk, r);
+        } else {
+          mbar_arrive(&ctl.full[slot]);
+        }
+        ++seq;
+      };
+#pragma unroll 1
+      for (int t = 0; t <= nt && !stop; ++t) {
+        if (t < nt) {
+          next_rows(t);
+#pragma unroll 1
+          for (int blk = 0; blk < 9; ++blk) produce(blk, own);
+        }
+        if (t >= 1) {
+          // value blocks of tile t-1: its rows are in prev[] (or still in own[]
+          // after the last tile)
+          const bool last = (t == nt);
+#pragma unroll 1
+          for (int pr = 0; pr < 4; ++pr) {
+            if (seq % S == S - 1) produce(-1, own);
+            produce(2 * pr, last ? own : prev);
+            produce(2 * pr + 1, last ? own : prev);
+          }
         }
       }
     }
@@ -372,84 +439,114 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ============================ MMA issue ==================================
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, NQ, false, false);
+      constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kKeys, NQ, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, NQ, true, false);
-      int seq = 0;
       bool ok = mbar_wait_spin(&ctl.q_full, 0, &ctl.abort, a.status);
       // cp.async writes shared memory through the generic proxy and the MMA
       // reads it through the async proxy: a proxy fence follows each acquire.
-      auto wait_full = [&](int& slot) -> bool {
-        slot = seq % S;
-        return mbar_wait_spin(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
-      };
       auto fences = [&]() {
         fence_proxy_async_smem();
         tc::fence_after_sync();
       };
-      auto take = [&](int& slot) -> bool {
-        const bool r = wait_full(slot);
-        fences();
-        return r;
+      // S^T (+)= K block (slot) . Q block blk^T
+      auto qk_block = [&](int slot, int blk, bool first) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t adesc = tc::smem_desc(sRing + slot * Cfg::kSlotBytes + k * 32, 16, 1024, tc::kSwizzle128B);
+          const uint64_t bdesc = tc::smem_desc(sQ + blk * Cfg::kQBlock + k * 32, 16, 1024, tc::kSwizzle128B);
+          tc::mma_bf16_ss(tmem + Cfg::kColS, adesc, bdesc, idesc_qk, (first && k == 0) ? 0u : 1u);
+        }
+      };
+      // O^T block m (+)= V^T (slots sa, sa+1) . P^T
+      auto pv_block = [&](int m, int sa, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t adesc =
+              tc::smem_desc(sRing + sa * Cfg::kSlotBytes + kk * 2048, Cfg::kSlotBytes, 1024, tc::kSwizzle128B);
+          const uint64_t bdesc =
+              tc::smem_desc(sP + (kk >> 2) * Cfg::kPRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
+          tc::mma_bf16_ss(tmem + m * Cfg::kOStride, adesc, bdesc, idesc_pv, (first && kk == 0) ? 0u : 1u);
+        }
       };
       // A slot is free again once the MMAs reading it are done.
       auto release = [&](int slot) { tc::mma_commit(&ctl.empty[slot]); };
+      if constexpr (kLandOnce) {
 #pragma unroll 1
-      for (int t = 0; t <= nt && ok; ++t) {
-        if (t < nt) {
-          // S^T(t) once the softmax has read S^T(t-1) out of TMEM.
-          if (t >= 1) {
-            ok = mbar_wait_spin(&ctl.s_free, (t - 1) & 1, &ctl.abort, a.status);
-            tc::fence_after_sync();
-            if (!ok) break;
-          }
+        for (int t = 0; t < nt && ok; ++t) {
+          // QK(t): block b from slot b, in the order PV(t-1) released them
 #pragma unroll 1
-          for (int blk = 0; blk < 9 && ok; ++blk) {
-            int slot;
-            if (!(ok = take(slot))) break;
-            ++seq;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t adesc = tc::smem_desc(sRing + slot * Cfg::kSlotBytes + k * 32, 16, 1024, tc::kSwizzle128B);
-              const uint64_t bdesc = tc::smem_desc(sQ + blk * Cfg::kQBlock + k * 32, 16, 1024, tc::kSwizzle128B);
-              tc::mma_bf16_ss(tmem + Cfg::kColS, adesc, bdesc, idesc_qk, (blk | k) ? 1u : 0u);
-            }
-            release(slot);
+          for (int blk = 0; blk < 9; ++blk) {
+            if (!(ok = mbar_wait_spin(&ctl.full[blk], t & 1, &ctl.abort, a.status))) break;
+            fences();
+            qk_block(blk, blk, blk == 0);
           }
           if (!ok) break;
-          tc::mma_commit(&ctl.s_full);
-        }
-        if (t >= 1) {
-          // O^T += V^T(t-1) . P^T(t-1)
-          const int u = t - 1;
-          ok = mbar_wait_spin(&ctl.p_full, u & 1, &ctl.abort, a.status);
+          tc::mma_commit(&ctl.s_full);  // also covers PV(t-1): O^T and slot 8 are the softmax's now
+          ok = mbar_wait_spin(&ctl.p_full, t & 1, &ctl.abort, a.status);
           tc::fence_after_sync();
+          if (!ok) break;
+          // PV(t), releasing each value pair after its M-block and slot 8 last
 #pragma unroll 1
-          for (int m = 0; m < 4 && ok; ++m) {
-            int sa, sb;
-            if (seq % S == S - 1) {  // filler slot: nothing to read
-              if (!(ok = wait_full(sa))) break;
-              release(sa);
-              ++seq;
-            }
-            // one fence after both halves of the pair have landed
-            if (!(ok = wait_full(sa))) break;
-            ++seq;
-            if (!(ok = wait_full(sb))) break;
-            ++seq;
-            fences();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t adesc =
-                  tc::smem_desc(sRing + sa * Cfg::kSlotBytes + kk * 2048, Cfg::kSlotBytes, 1024, tc::kSwizzle128B);
-              const uint64_t bdesc =
-                  tc::smem_desc(sP + (kk >> 2) * Cfg::kPRegion + (kk & 3) * 32, 16, 1024,
-                                tc::kSwizzle128B);
-              tc::mma_bf16_ss(tmem + m * Cfg::kOStride, adesc, bdesc, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
-            }
-            release(sa);
-            release(sb);
+          for (int m = 0; m < 4; ++m) {
+            pv_block(m, 2 * m, t == 0);
+            release(2 * m);
+            release(2 * m + 1);
           }
-          if (ok) tc::mma_commit(&ctl.pv_done[u & 1]);
+          release(8);
+        }
+        if (ok) tc::mma_commit(&ctl.pv_last);
+      } else {
+        int seq = 0;
+        auto wait_full = [&](int& slot) -> bool {
+          slot = seq % S;
+          return mbar_wait_spin(&ctl.full[slot], (seq / S) & 1, &ctl.abort, a.status);
+        };
+#pragma unroll 1
+        for (int t = 0; t <= nt && ok; ++t) {
+          if (t < nt) {
+            // S^T(t) once the softmax has read S^T(t-1) out of TMEM.
+            if (t >= 1) {
+              ok = mbar_wait_spin(&ctl.s_free, (t - 1) & 1, &ctl.abort, a.status);
+              tc::fence_after_sync();
+              if (!ok) break;
+            }
+#pragma unroll 1
+            for (int blk = 0; blk < 9 && ok; ++blk) {
+              int slot;
+              if (!(ok = wait_full(slot))) break;
+              fences();
+              ++seq;
+              qk_block(slot, blk, blk == 0);
+              release(slot);
+            }
+            if (!ok) break;
+            tc::mma_commit(&ctl.s_full);
+          }
+          if (t >= 1) {
+            // O^T += V^T(t-1) . P^T(t-1)
+            const int u = t - 1;
+            ok = mbar_wait_spin(&ctl.p_full, u & 1, &ctl.abort, a.status);
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int m = 0; m < 4 && ok; ++m) {
+              int sa, sb;
+              if (seq % S == S - 1) {  // filler slot: nothing to read
+                if (!(ok = wait_full(sa))) break;
+                release(sa);
+                ++seq;
+              }
+              // one fence after both halves of the pair have landed
+              if (!(ok = wait_full(sa))) break;
+              ++seq;
+              if (!(ok = wait_full(sb))) break;
+              ++seq;
+              fences();
+              pv_block(m, sa, u == 0);
+              release(sa);
+              release(sb);
+            }
+            if (ok) tc::mma_commit(&ctl.pv_done[u & 1]);
+          }
         }
       }
       // Drain: every MMA this thread issued has completed before TMEM is freed.
@@ -482,7 +579,7 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
     bool my_abort = false;
 #pragma unroll 1
     for (int t = 0; t < nt; ++t) {
-      const int64_t key = j0 + (int64_t)tile_at(t) * kKeysPerTile + j;
+      const int64_t key = j0 + (int64_t)tile_at(t) * kKeys + j;
       uint64_t vis = 0;
       if (key < j1 && resolve_row(a, rq.q0, P, kv_base, key) >= 0) {  // rows outside the pool are excluded
         for (int tl = 0; tl < ntok; ++tl)
@@ -502,7 +599,9 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0 && !my_abort) mbar_arrive(&ctl.s_free);  // S^T may be overwritten now
+      // S^T may be overwritten now (resident mode: QK(t+1) follows PV(t), which
+      // waits for P^T(t), so no separate signal is needed)
+      if (!kLandOnce && lane == 0 && !my_abort) mbar_arrive(&ctl.s_free);
 
       bool need = false;
       const float4* mt4 = reinterpret_cast<const float4*>(&ctl.mtau[c0]);
@@ -554,8 +653,8 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         rescale = (t > 0) && ctl.rflag[t & 1];
       }
       // P^T(t) overwrites what PV(t-1) reads, and a rescale of O^T needs
-      // PV(t-1) complete as well.
-      if (t >= 1 && !my_abort)
+      // PV(t-1) complete as well (resident mode: S^T(t) completing implies it).
+      if (!kLandOnce && t >= 1 && !my_abort)
         my_abort = !mbar_wait(&ctl.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, &ctl.abort, a.status);
       my_abort = __any_sync(0xffffffffu, my_abort);
       tc::fence_after_sync();
@@ -628,10 +727,22 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
         }
         l_half += a0 + a1;
       }
+      if constexpr (kLandOnce) {
+        // slot 8 may take the next tile's RoPE block once PV and these reads are done
+        if (tid < 2 * NQ && !my_abort) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.empty[8]);
+        }
+      }
     }
 
     // ---- epilogue: l, LSE, O = O^T / l ----------------------------------------
-    if (!my_abort) my_abort = !mbar_wait(&ctl.pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, &ctl.abort, a.status);
+    if (!my_abort) {
+      if constexpr (kLandOnce)
+        my_abort = !mbar_wait(&ctl.pv_last, 0, &ctl.abort, a.status);
+      else
+        my_abort = !mbar_wait(&ctl.pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, &ctl.abort, a.status);
+    }
     tc::fence_after_sync();
     const bool wa = __any_sync(0xffffffffu, my_abort) || ctl.abort;
     if (lane == 0) ctl.flag[nt & 1][warp] = wa ? 2 : 0;
@@ -704,16 +815,17 @@ __global__ void __launch_bounds__(TcCfg<NQ>::kThreads, 1)
   }
 }
 
-template <int NQ>
+template <int NQ, int kMode>
 cudaError_t launch_split_tc_nq(const SplitArgs& a, const TcMaps& maps, dim3 grid, cudaStream_t stream) {
-  constexpr int smem = tc_smem_bytes<NQ>();
+  constexpr int smem = tc_smem_bytes<NQ, kMode>();
   static_assert(smem <= 232448, "shared memory budget exceeded");
-  void (*kernel)(SplitArgs, TcMaps) = a.merge_count ? split_tc_kernel<NQ, true> : split_tc_kernel<NQ, false>;
+  void (*kernel)(SplitArgs, TcMaps) =
+      a.merge_count ? split_tc_kernel<NQ, true, kMode> : split_tc_kernel<NQ, false, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(TcCfg<NQ>::kThreads, 1, 1);
+  cfg.blockDim = dim3(TcCfg<NQ, kMode>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = nullptr;

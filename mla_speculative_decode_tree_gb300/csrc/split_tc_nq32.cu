@@ -1,9 +1,13 @@
-// Tensor-core split kernel instantiated for 32 query rows per CTA.
+// Tensor-core split kernel instantiated for 32 query rows per CTA, in both
+// modes (value blocks fetched twice, or the whole tile resident).
 #include "split_tc.cuh"
 
 namespace mlav {
-cudaError_t launch_split_tc_32(const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t stream) {
-  return launch_split_tc_nq<32>(a, m, grid, stream);
+cudaError_t launch_split_tc_32(const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t stream, bool resident) {
+  return resident ? launch_split_tc_nq<32, kResident>(a, m, grid, stream)
+                  : launch_split_tc_nq<32, kRefetch>(a, m, grid, stream);
 }
-int split_tc_smem_32() { return tc_smem_bytes<32>(); }
+int split_tc_smem_32(bool resident) {
+  return resident ? tc_smem_bytes<32, kResident>() : tc_smem_bytes<32, kRefetch>();
+}
 }  // namespace mlav

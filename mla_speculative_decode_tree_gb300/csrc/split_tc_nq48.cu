@@ -1,9 +1,13 @@
-// Tensor-core split kernel instantiated for 48 query rows per CTA.
+// Tensor-core split kernel instantiated for 48 query rows per CTA, in both
+// modes (value blocks fetched twice, or the whole tile resident).
 #include "split_tc.cuh"
 
 namespace mlav {
-cudaError_t launch_split_tc_48(const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t stream) {
-  return launch_split_tc_nq<48>(a, m, grid, stream);
+cudaError_t launch_split_tc_48(const SplitArgs& a, const TcMaps& m, dim3 grid, cudaStream_t stream, bool resident) {
+  return resident ? launch_split_tc_nq<48, kResident>(a, m, grid, stream)
+                  : launch_split_tc_nq<48, kRefetch>(a, m, grid, stream);
 }
-int split_tc_smem_48() { return tc_smem_bytes<48>(); }
+int split_tc_smem_48(bool resident) {
+  return resident ? tc_smem_bytes<48, kResident>() : tc_smem_bytes<48, kRefetch>();
+}
 }  // namespace mlav

@@ -90,7 +90,7 @@ def test_plan_accepts_the_test_stall_flag(lib):
     (dict(pool_rows=0), B.MLA_VERIFY_EINVAL),
     (dict(max_kv_len=3), B.MLA_VERIFY_EINVAL),
     (dict(flags=0x200), B.MLA_VERIFY_EINVAL),
-    (dict(flags=0x4), B.MLA_VERIFY_EINVAL),
+    (dict(flags=0x8), B.MLA_VERIFY_EINVAL),
 ])
 def test_plan_rejects(lib, kw, code):
     with pytest.raises(B.MlaVerifyError) as e:
@@ -108,19 +108,26 @@ def test_plan_null_pointers(lib):
     assert lib.mla_verify_destroy(None) == B.MLA_VERIFY_OK
 
 
-@pytest.mark.parametrize("H,T,kv,ns,flags,kernel,nq", [
-    (64, 9, 65545, 64, 0, 1, 96),  # 576 rows, 64 splits: 384 CTAs, more than one wave -> least work
-    (64, 9, 65545, 16, 0, 1, 64),  # 16 splits: 96 CTAs -> 9 x 16 = 144 fit one wave (48 rows: 192)
-    (64, 9, 5009, 16, 0, 1, 64),   # 14 splits: 84 CTAs -> 9 x 14 = 126 (48 rows: 168)
-    (64, 9, 4105, 16, 0, 1, 48),   # 11 splits: 66 CTAs -> 12 x 11 = 132
-    (8, 9, 5009, 16, 0, 1, 48),    # 72 rows: 1 group of 96 -> 2 groups of 48 (28 CTAs)
-    (16, 4, 5004, 16, 0, 1, 48),   # 64 rows -> 48 + 16
-    (8, 1, 5001, 16, 0, 1, 16),    # decode with 8 heads: 16-row tile, half padding, still tensor cores
-    (64, 9, 5009, 16, B.MLA_VERIFY_FORCE_SIMT, 0, 8),
+R = B.MLA_VERIFY_REFETCH_VALUES
+
+
+@pytest.mark.parametrize("H,T,kv,ns,flags,kernel,res,nq", [
+    # 576 rows, 64 splits: 342 CTAs at 96 rows (3 waves) beat 513 resident 64-row CTAs (4 waves)
+    (64, 9, 65545, 64, 0, 1, 0, 96),
+    (64, 9, 65545, 16, 0, 1, 1, 64),   # 16 splits of 33 tiles: 144 resident CTAs fill one wave
+    (64, 9, 5009, 16, 0, 1, 1, 64),    # 14 splits: 9 x 14 = 126 CTAs (48 rows: 168, two waves)
+    (64, 9, 4105, 16, 0, 1, 1, 64),    # 11 splits: 99 CTAs; 48 rows (132) would land each key 12 times
+    (8, 9, 5009, 16, 0, 1, 1, 48),     # 72 rows: 2 resident groups of 48
+    (16, 4, 5004, 16, 0, 1, 1, 64),    # 64 rows: one resident group
+    (8, 1, 5001, 16, 0, 1, 1, 16),     # decode with 8 heads: 16-row tile, half padding, still tensor cores
+    (64, 9, 4105, 16, R, 1, 0, 48),    # value-refetch mode: one wave at 48 rows (more ring slots)
+    (8, 9, 185009, 64, R, 1, 0, 48),   # 72 rows, 63 splits: 2 x 63 = 126 CTAs in one wave
+    (64, 9, 5009, 16, B.MLA_VERIFY_FORCE_SIMT, 0, 0, 8),
 ])
-def test_plan_kernel_choice(lib, H, T, kv, ns, flags, kernel, nq):
+def test_plan_kernel_choice(lib, H, T, kv, ns, flags, kernel, res, nq):
     info = plan(num_heads=H, q_len=T, max_kv_len=kv, nsplit=ns, flags=flags).describe()
     assert info.kernel == kernel
+    assert info.resident_tile == res
     assert info.rows_per_cta == nq
     assert info.grid_x == -(-(H * T) // nq)
     assert info.grid_y == ns and info.grid_z == 1
@@ -191,14 +198,16 @@ def test_auto_split_plan(lib):
     assert run_raw(lib, p, nsplit=0, batch=0) == B.MLA_VERIFY_OK
 
 
-@pytest.mark.parametrize("B_,H,T,kv,nq,splits", [
-    (1, 64, 9, 4105, 96, 17),     # short4k: one wave of 102 CTAs, 2 tiles each
-    (1, 64, 9, 65545, 96, 25),    # mid64k: one wave of 150 CTAs
-    (1, 8, 9, 185009, 96, 145),   # long185k_h8: one row group, 145 CTAs of 10 tiles
+@pytest.mark.parametrize("B_,H,T,kv,res,nq,splits", [
+    (1, 64, 9, 4105, 0, 96, 17),     # short4k: one wave of 102 CTAs, 2 tiles each
+    (1, 64, 9, 65545, 0, 96, 25),    # mid64k: one wave of 150 CTAs
+    (1, 8, 9, 185009, 0, 96, 145),   # long185k_h8: one row group, 145 CTAs of 10 tiles
+    (16, 64, 1, 32769, 1, 64, 26),   # decode, 16 requests: one resident 64-row group each
 ])
-def test_auto_split_choices_on_152_sms(lib, B_, H, T, kv, nq, splits):
-    """The cost model's picks for single requests on a 152-SM GB300 (the host
-    fallback count when no device answers)."""
+def test_auto_split_choices_on_152_sms(lib, B_, H, T, kv, res, nq, splits):
+    """The cost model's picks on a 152-SM GB300 (the host fallback count when
+    no device answers)."""
     info = plan(max_batch=B_, num_heads=H, q_len=T, max_kv_len=kv, pool_rows=1 << 20, nsplit=0).describe()
-    assert (info.rows_per_cta, info.grid_y) == (nq, splits)
-    assert -(-H * T // nq) * splits * B_ <= 152
+    assert (info.resident_tile, info.rows_per_cta, info.grid_y) == (res, nq, splits)
+    if B_ == 1:
+        assert -(-H * T // nq) * splits <= 152

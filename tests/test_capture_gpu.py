@@ -31,7 +31,8 @@ def _fill(buf, arr, dtype):
     buf[: t.numel()].copy_(t.reshape(-1))
 
 
-@pytest.mark.parametrize("H,flags", [(64, 0), (8, 0), (64, B.MLA_VERIFY_FORCE_SIMT)])
+@pytest.mark.parametrize("H,flags", [(64, 0), (8, 0), (64, B.MLA_VERIFY_REFETCH_VALUES), (8, B.MLA_VERIFY_REFETCH_VALUES),
+                                     (64, B.MLA_VERIFY_FORCE_SIMT)])
 def test_capture_then_replay_with_new_inputs(H, flags):
     from oracle import ref
     T, pool_rows, cap = 9, 8192, 2000

@@ -26,11 +26,12 @@ def built():
     build.build()
 
 
-def test_stalled_pipeline_times_out_and_the_context_stays_usable():
+@pytest.mark.parametrize("mode", [0, B.MLA_VERIFY_REFETCH_VALUES], ids=["resident", "refetch"])
+def test_stalled_pipeline_times_out_and_the_context_stays_usable(mode):
     from oracle import ref
     wl = W.tiny_workload(B=1, H=16, T=4, prefix_lens=[600], pool_rows=4096, seed=3, nsplit=2)
     d = B.device_inputs(wl)
-    v = B.verifier_for(wl, flags=B.MLA_VERIFY_TEST_STALL_GATHER)
+    v = B.verifier_for(wl, flags=B.MLA_VERIFY_TEST_STALL_GATHER | mode)
     assert v.plan.describe().kernel == 1
     torch.cuda.synchronize()
     t0 = time.time()
@@ -41,7 +42,7 @@ def test_stalled_pipeline_times_out_and_the_context_stays_usable():
     assert st & B.MLA_VERIFY_DEV_TIMEOUT, st
     assert 0.5 < dt < 60, dt  # the waits are bounded at about 2 s
 
-    good = B.verifier_for(wl)
+    good = B.verifier_for(wl, flags=mode)
     o, lse = good.run(d, wl["B"], wl["sm_scale"])
     torch.cuda.synchronize()
     assert good.status() == 0

@@ -24,9 +24,9 @@ def built():
     build.build()
 
 
-def _pair(wl, nsplit=None):
-    plain = B.verifier_for(wl, nsplit=nsplit)
-    fused = B.verifier_for(wl, nsplit=nsplit, flags=B.MLA_VERIFY_FUSED_MERGE)
+def _pair(wl, nsplit=None, mode=0):
+    plain = B.verifier_for(wl, nsplit=nsplit, flags=mode)
+    fused = B.verifier_for(wl, nsplit=nsplit, flags=B.MLA_VERIFY_FUSED_MERGE | mode)
     assert fused.plan.describe().merge_blocks == 0 and fused.plan.describe().kernel == 1
     return plain, fused
 
@@ -46,12 +46,13 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("mode", [0, B.MLA_VERIFY_REFETCH_VALUES], ids=["resident", "refetch"])
 @pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
-def test_fused_equals_separate_merge(case):
+def test_fused_equals_separate_merge(case, mode):
     Bn, H, T, P, nsplit = case
     wl = W.tiny_workload(B=Bn, H=H, T=T, prefix_lens=P, pool_rows=32768, seed=Bn * 7 + H + T, nsplit=nsplit)
     d = B.device_inputs(wl)
-    plain, fused = _pair(wl)
+    plain, fused = _pair(wl, mode=mode)
     fused.o.fill_(float("nan"))
     plain.run(d, wl["B"], wl["sm_scale"])
     fused.run(d, wl["B"], wl["sm_scale"])

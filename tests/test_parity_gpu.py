@@ -19,6 +19,10 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 NTHREADS = os.cpu_count() or 4
+# Tensor-core kernel in resident-tile mode (the default), in value-refetch
+# mode, and the CUDA-core kernel.
+MODES = [0, B.MLA_VERIFY_REFETCH_VALUES, B.MLA_VERIFY_FORCE_SIMT]
+MODE_IDS = ["resident", "refetch", "simt"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,7 +59,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("flags", [0, B.MLA_VERIFY_FORCE_SIMT], ids=["auto", "simt"])
+@pytest.mark.parametrize("flags", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("name", [s[0] for s in SMALL])
 def test_parity_small_configs(name, flags):
     wl = W.make_workload(W.CONFIGS[name])
@@ -65,25 +69,26 @@ def test_parity_small_configs(name, flags):
 ADHOC = [
     # B, H, T, prefixes, pool, nsplit, tree
     (3, 64, 9, [0, 127, 1000], 4096, 4, "random"),   # empty prefix, ragged tail, multi-tile
-    (2, 8, 9, [128, 385], 2048, 3, "random"),        # H=8: 72 rows, small grid -> 48-row groups
+    (2, 8, 9, [128, 385], 2048, 3, "random"),        # H=8: 72 rows, small grid
     (2, 16, 4, [256, 255], 2048, 2, "chain"),        # 64 rows
     (1, 64, 1, [700], 2048, 2, "random"),            # decode (T=1) on the tensor cores
     (2, 8, 1, [300, 5], 2048, 2, "random"),          # decode with 8 rows: half-empty 16-row tile
     (2, 5, 7, [200, 333], 2048, 3, "random"),        # 35 rows -> 48-row group, tokens straddle groups
     (1, 1, 16, [90], 1024, 1, "random"),             # 16 rows, one head
     (1, 32, 3, [5000], 8192, 64, "random"),          # more splits than needed: empty splits
-    (2, 96, 2, [130, 129], 2048, 2, "random"),       # 192 rows = 2 x 96
-    # one case per row-group size the planner can pick (the fill-aware choice
-    # moves small grids to 48 rows, so the others need grids of >= 152 CTAs)
+    (2, 96, 2, [130, 129], 2048, 2, "random"),       # 192 rows = 3 x 64 or 2 x 96
+    # one case per row-group size the planner can pick in each mode (the
+    # fill-aware choice moves small grids to 48 rows, so the others need grids
+    # of >= 152 CTAs)
     (2, 8, 4, [300, 77], 2048, 2, "random"),          # 32 rows -> 32-row groups
     (3, 16, 4, [2000, 300, 4000], 8192, 64, "random"),  # 64 rows, 192 CTAs -> 64-row groups
-    (4, 8, 9, [3000, 100, 5000, 64], 16384, 64, "random"),  # 72 rows, 256 CTAs -> one 96-row group
-    (2, 64, 9, [5000, 3000], 16384, 64, "random"),    # 576 rows, 480 CTAs -> 96-row groups
+    (4, 8, 9, [3000, 100, 5000, 64], 16384, 64, "random"),  # 72 rows, 256 CTAs -> 48 rows, or one 96-row group
+    (2, 64, 9, [5000, 3000], 16384, 64, "random"),    # 576 rows -> 64-row groups, or 96
     (1, 2, 64, [500], 4096, 2, "random"),             # q_len 64 (the maximum): 24 tokens per group
 ]
 
 
-@pytest.mark.parametrize("flags", [0, B.MLA_VERIFY_FORCE_SIMT], ids=["auto", "simt"])
+@pytest.mark.parametrize("flags", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("case", ADHOC, ids=[str(i) for i in range(len(ADHOC))])
 def test_parity_adhoc(case, flags):
     Bn, H, T, prefixes, pool, nsplit, tree = case
@@ -92,12 +97,17 @@ def test_parity_adhoc(case, flags):
     check_full(wl, flags, what=str(case))
 
 
-def test_every_row_group_size_is_exercised():
-    sizes = set()
-    for B_, H, T, prefixes, pool, nsplit, tree in ADHOC:
-        L = max(prefixes) + T
-        sizes.add(B.mla_verify_plan(B_, H, T, L, pool, nsplit).describe().rows_per_cta)
-    assert {16, 32, 48, 64, 96} <= sizes, sizes
+def test_every_mode_and_row_group_size_is_exercised():
+    """The ad-hoc cases, planned with and without MLA_VERIFY_REFETCH_VALUES,
+    cover every (mode, rows per CTA) pair the planner can pick."""
+    pairs = set()
+    for flags in MODES[:2]:
+        for B_, H, T, prefixes, pool, nsplit, tree in ADHOC:
+            info = B.mla_verify_plan(B_, H, T, max(prefixes) + T, pool, nsplit, flags).describe()
+            assert info.kernel == 1 and not (flags and info.resident_tile)
+            pairs.add((info.resident_tile, info.rows_per_cta))
+    want = {(1, n) for n in (16, 32, 48, 64)} | {(0, n) for n in (16, 32, 48, 64, 96)}
+    assert want <= pairs, want - pairs
 
 
 FULL = ["short4k", "mid64k", "long185k_h8", "batch16_ragged", "needle64k"]
@@ -112,12 +122,13 @@ def full_workload(name):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("flags", MODES[:2], ids=MODE_IDS[:2])
 @pytest.mark.parametrize("name", FULL)
-def test_parity_full_configs_sampled(name):
+def test_parity_full_configs_sampled(name, flags):
     from oracle import ref
     wl = full_workload(name)
     rows = sample_rows(wl, per_request=36 if wl["B"] == 1 else 6)
-    o, lse, st, v = gpu_run(wl)
+    o, lse, st, v = gpu_run(wl, flags=flags)
     assert st == 0
     o_ref, lse_ref = ref.verify(wl, rows=rows, nthreads=NTHREADS)
     err = compare(o[rows], lse[rows], o_ref, lse_ref, name)
@@ -137,13 +148,14 @@ def test_short4k_simt_cross_check():
 
 
 @pytest.mark.slow
-def test_locality_pair_bit_identical():
+@pytest.mark.parametrize("flags", MODES[:2], ids=MODE_IDS[:2])
+def test_locality_pair_bit_identical(flags):
     """Scattered rows vs a sorted free list holding the same logical rows: identical bits."""
     from oracle import ref
     wl = W.make_workload(W.CONFIGS["mid64k"])
     wl_sorted = W.relayout(wl, "sorted", seed=1234)
-    o1, lse1, st1, _ = gpu_run(wl)
-    o2, lse2, st2, _ = gpu_run(wl_sorted)
+    o1, lse1, st1, _ = gpu_run(wl, flags=flags)
+    o2, lse2, st2, _ = gpu_run(wl_sorted, flags=flags)
     assert st1 == 0 and st2 == 0
     assert np.array_equal(o1, o2) and np.array_equal(lse1, lse2)
     rows = sample_rows(wl, per_request=12)
@@ -151,11 +163,12 @@ def test_locality_pair_bit_identical():
     compare(o2[rows], lse2[rows], o_ref, lse_ref, "sorted layout")
 
 
+@pytest.mark.parametrize("flags", MODES[:2], ids=MODE_IDS[:2])
 @pytest.mark.parametrize("nsplit", [1, 2, 5, 16, 64])
-def test_nsplit_invariance(nsplit):
+def test_nsplit_invariance(nsplit, flags):
     from oracle import ref
     wl = W.tiny_workload(B=2, H=64, T=9, prefix_lens=[3000, 1200], pool_rows=8192, seed=21, nsplit=nsplit)
-    o, lse, st, _ = gpu_run(wl)
+    o, lse, st, _ = gpu_run(wl, flags=flags)
     o_ref, lse_ref = ref.verify(wl, nthreads=NTHREADS)
     compare(o, lse, o_ref, lse_ref, "nsplit=%d" % nsplit)
 
@@ -172,7 +185,7 @@ def encoded_pool(pool_rows, rng):
     return W.f32_to_bf16_bits(pool)
 
 
-@pytest.mark.parametrize("flags", [0, B.MLA_VERIFY_FORCE_SIMT], ids=["auto", "simt"])
+@pytest.mark.parametrize("flags", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("H,T,prefixes", [(64, 9, [300, 1001, 7]), (8, 9, [129, 0, 640]), (3, 5, [40, 9, 300])])
 def test_row_selection_and_mask_decoding_exact(H, T, prefixes, flags):
     """One visible key per draft token at a chosen position: O must be that row, bit for bit."""
@@ -213,7 +226,7 @@ def test_bad_row_sets_status_and_is_excluded():
     wl = W.tiny_workload(B=2, H=16, T=4, prefix_lens=[200, 150], pool_rows=1024, seed=5)
     bad = wl["kv_indices"].copy()
     bad[17] = 5000  # request 0, prefix key 17
-    for flags in (0, B.MLA_VERIFY_FORCE_SIMT):
+    for flags in MODES:
         o, lse, st, _ = gpu_run(dict(wl, kv_indices=bad), flags=flags)
         assert st & B.MLA_VERIFY_DEV_BAD_ROW
         # reference: the same call with key 17 of request 0 masked for every token
@@ -278,7 +291,7 @@ AUTO_SPLIT = [
 ]
 
 
-@pytest.mark.parametrize("flags", [0, B.MLA_VERIFY_FORCE_SIMT], ids=["auto", "simt"])
+@pytest.mark.parametrize("flags", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("case", AUTO_SPLIT, ids=[str(i) for i in range(len(AUTO_SPLIT))])
 def test_parity_auto_split(case, flags):
     Bn, H, T, prefixes, pool = case

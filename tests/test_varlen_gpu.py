@@ -55,7 +55,8 @@ VARLEN = [
 ]
 
 
-@pytest.mark.parametrize("flags", [0, B.MLA_VERIFY_FORCE_SIMT], ids=["auto", "simt"])
+@pytest.mark.parametrize("flags", [0, B.MLA_VERIFY_REFETCH_VALUES, B.MLA_VERIFY_FORCE_SIMT],
+                         ids=["resident", "refetch", "simt"])
 @pytest.mark.parametrize("case", VARLEN, ids=[str(i) for i in range(len(VARLEN))])
 def test_varlen_parity(case, flags):
     H, T_list, prefixes, nsplit = case
