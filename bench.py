@@ -57,6 +57,20 @@ def workload_desc(cfg) -> str:
             % (cfg.name, cfg.B, cfg.H, cfg.T, cfg.tree, pre, cfg.pool_rows, cfg.nsplit, cfg.layout))
 
 
+def gpu_config(cfg, nsplit, chunks, world) -> dict:
+    """The GPU arm's ``config``: the workload and how it is timed."""
+    return {"workload": workload_desc(cfg) + ("" if nsplit is None else
+                                              " (run with nsplit=%d: %d chunks)" % (nsplit, chunks)),
+            "l2": "flushed (512 MiB write) before every step",
+            "parallelism": "replicas" if world > 1 else "single GPU", "graph": "split+merge in one CUDA graph"}
+
+
+def reference_config(cfg, cores) -> dict:
+    """The reference arm's ``config``: the GPU arm's keys, the same workload."""
+    return {"workload": workload_desc(cfg), "l2": "not applicable (fp64 CPU oracle on the host)",
+            "parallelism": "%d host threads" % cores, "graph": "none (no reference code exists to install)"}
+
+
 def algorithmic(wl):
     """Algorithmic bytes and FLOPs of one verify call (and of its split kernel)."""
     H = wl["H"]
@@ -547,10 +561,7 @@ def run_gpu(args):
         "metric": METRIC, "value": round(us_call, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg) + ("" if args.nsplit is None else
-                                                      " (run with nsplit=%d: %d chunks)" % (args.nsplit, info.grid_y)),
-                   "l2": "flushed (512 MiB write) before every step",
-                   "parallelism": "replicas" if world > 1 else "single GPU", "graph": "split+merge in one CUDA graph"},
+        "config": gpu_config(cfg, args.nsplit, info.grid_y, world),
         "us_per_call_median": round(float(np.median(step_ms)) * 1e3, 3),
         "us_per_call_p10_p90": [round(float(np.percentile(step_ms, 10)) * 1e3, 3),
                                 round(float(np.percentile(step_ms, 90)) * 1e3, 3)],
@@ -692,7 +703,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "what": "fp64 CPU oracle (no reference code exists to install)"},
+        "config": reference_config(cfg, cores),
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d of %d output rows per step, scaled to a whole call" % (sample, n_all)},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

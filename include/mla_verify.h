@@ -326,15 +326,19 @@ int mla_verify_relocate_kv(mla_verify_plan_t plan, void* kv_pool, const int32_t*
  * library, which every GPU that loads the library keeps reserved until the
  * process exits.  A plan whose workspace_bytes exceeds 32 MiB is rejected
  * with MLA_VERIFY_EWORKSPACE (e.g. 64 heads x 9 draft tokens fit up to
- * nsplit = 28 at batch 1).  Nothing is allocated: the first call on a device
- * looks up the array's device address (cudaGetSymbolAddress, with that device
- * current), so make that first call outside any stream capture.  Each call
- * zeroes the array's 256-byte status header on `stream` and then runs exactly
- * mla_verify_run on it.  All calls in the process share the one array: calls
- * whose work overlaps on the GPU (other streams, other threads) race and
- * corrupt each other's results; serialise them.  Device-detected conditions
- * are not reported (there is no workspace to read a status word from).
- * Arguments and errors otherwise as mla_verify_run.
+ * nsplit = 28 at batch 1).  Nothing is allocated: the first call in each CUDA
+ * context (the device's primary context, or a context the caller made
+ * current) looks up the array's device address in that context
+ * (cudaGetSymbolAddress), so make that first call outside any stream capture;
+ * a process may use up to 64 contexts this way (then EUNSUPPORTED).  Each
+ * call first makes every check of mla_verify_run (a rejected call touches
+ * nothing on the device), then zeroes the array's 256-byte status header and,
+ * for a MLA_VERIFY_FUSED_MERGE plan, its arrival counters, on `stream`, and
+ * runs exactly mla_verify_run on the array.  All calls in the process share
+ * the one array: calls whose work overlaps on the GPU (other streams, other
+ * threads) race and corrupt each other's results; serialise them.
+ * Device-detected conditions are not reported (there is no workspace to read
+ * a status word from).  Arguments and errors otherwise as mla_verify_run.
  */
 int mla_verify_run_noalloc(mla_verify_plan_t plan, const void* q_nope_absorbed, const void* q_rope,
                            const void* kv_pool, const int32_t* kv_indptr, const int32_t* kv_indices,

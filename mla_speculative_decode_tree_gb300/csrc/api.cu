@@ -219,6 +219,22 @@ int check_device() {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The input arrays of a split launch (everything but the workspace).
+int check_inputs(const void* q_nope_absorbed, const void* q_rope, const void* kv_pool, const int32_t* kv_indptr,
+                 const int32_t* kv_indices, const int32_t* out_cache_loc, const uint8_t* custom_mask,
+                 const int32_t* mask_indptr, float sm_scale) {
+  if (!q_nope_absorbed || !q_rope || !kv_pool || !kv_indptr || !out_cache_loc || !custom_mask || !mask_indptr)
+    return MLA_VERIFY_EINVAL;
+  // kv_indices may be NULL only when every prefix is empty; the device never
+  // reads it then.
+  if (!aligned(q_nope_absorbed, 16) || !aligned(q_rope, 16) || !aligned(kv_pool, 16) || !aligned(kv_indptr, 4) ||
+      (kv_indices && !aligned(kv_indices, 4)) || !aligned(out_cache_loc, 4) || !aligned(mask_indptr, 4))
+    return MLA_VERIFY_EINVAL;
+  if (!std::isfinite(sm_scale)) return MLA_VERIFY_EINVAL;
+  return MLA_VERIFY_OK;
+}
+
+
 int check_common(const mla_verify_plan_s* pl, int32_t batch, int32_t nsplit, void* ws, size_t ws_bytes) {
   if (!pl) return MLA_VERIFY_EINVAL;
   if (batch < 0 || batch > pl->p.max_batch) return MLA_VERIFY_EINVAL;
@@ -238,6 +254,23 @@ int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 // Bytes at the start of a plan's workspace that must be zero between calls
 // (status header and, for a fused merge, the arrival counters).
 size_t plan_zero_bytes(const mla_verify_plan_s* pl) { return pl->off_lse; }
+size_t plan_workspace_bytes(const mla_verify_plan_s* pl) { return pl->ws_bytes; }
+// Every check mla_verify_run makes before it enqueues work, except the
+// workspace ones: plan, batch range, nsplit, inputs, outputs, device.  The
+// no-allocation entry point runs it before it touches its scratch array.
+int check_run_args(const mla_verify_plan_s* pl, const void* q_nope_absorbed, const void* q_rope,
+                   const void* kv_pool, const int32_t* kv_indptr, const int32_t* kv_indices,
+                   const int32_t* out_cache_loc, const uint8_t* custom_mask, const int32_t* mask_indptr,
+                   int32_t batch, float sm_scale, int32_t nsplit, const void* o, const float* lse) {
+  if (!pl) return MLA_VERIFY_EINVAL;
+  if (batch < 0 || batch > pl->p.max_batch || nsplit != pl->p.nsplit) return MLA_VERIFY_EINVAL;
+  if (batch == 0) return MLA_VERIFY_OK;
+  if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return MLA_VERIFY_EINVAL;
+  int rc = check_inputs(q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, out_cache_loc, custom_mask,
+                        mask_indptr, sm_scale);
+  if (rc != MLA_VERIFY_OK) return rc;
+  return check_device();
+}
 }  // namespace mlav
 
 extern "C" {
@@ -325,14 +358,9 @@ int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_
   int rc = check_common(pl, batch, nsplit, workspace, workspace_bytes);
   if (rc != MLA_VERIFY_OK || batch == 0) return rc;
   if (pl->fused && (!o || !lse)) return MLA_VERIFY_EINVAL;  // a fused plan has no split-only call
-  if (!q_nope_absorbed || !q_rope || !kv_pool || !kv_indptr || !out_cache_loc || !custom_mask || !mask_indptr)
-    return MLA_VERIFY_EINVAL;
-  // kv_indices may be NULL only when every prefix is empty; the device never
-  // reads it then.
-  if (!aligned(q_nope_absorbed, 16) || !aligned(q_rope, 16) || !aligned(kv_pool, 16) || !aligned(kv_indptr, 4) ||
-      (kv_indices && !aligned(kv_indices, 4)) || !aligned(out_cache_loc, 4) || !aligned(mask_indptr, 4))
-    return MLA_VERIFY_EINVAL;
-  if (!std::isfinite(sm_scale)) return MLA_VERIFY_EINVAL;
+  if ((rc = check_inputs(q_nope_absorbed, q_rope, kv_pool, kv_indptr, kv_indices, out_cache_loc, custom_mask,
+                         mask_indptr, sm_scale)) != MLA_VERIFY_OK)
+    return rc;
   if ((rc = check_device()) != MLA_VERIFY_OK) return rc;
 
   SplitArgs a;

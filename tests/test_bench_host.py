@@ -44,3 +44,11 @@ def test_source_hash_ignores_comments_and_other_kernels(tmp_path):
 def test_traffic_keys():
     assert bench.traffic_key("mid64k") == "mid64k"
     assert bench.traffic_key("mid64k", 0) == "mid64k@nsplit0"
+
+
+def test_reference_arm_config_has_the_gpu_arms_keys():
+    from mla_speculative_decode_tree_gb300 import workloads as W
+    cfg = W.CONFIGS["short4k"]
+    g = bench.gpu_config(cfg, None, 16, 1)
+    r = bench.reference_config(cfg, 16)
+    assert set(g) == set(r) and g["workload"] == r["workload"]
