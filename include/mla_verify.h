@@ -104,8 +104,11 @@ typedef struct {
   int32_t q_len;      /* T in [1, 64]: draft tokens per request (uniform) */
   int32_t max_kv_len; /* >= max_b (P_b + T); documents the longest request (chunk size is per request) */
   int64_t pool_rows;  /* rows in kv_pool; keys resolving outside [0, pool_rows) are left out and flagged */
-  int32_t nsplit;     /* >= 1: KV chunks per request (chunk = ceil(L_b/nsplit) rounded up to 128 keys)
-                       *       = partials per output row (fixed grid dimension);
+  int32_t nsplit;     /* >= 1: KV chunks per request = partials per output row (fixed grid
+                       *       dimension); request b's chunk is ceil(L_b/nsplit) rounded up to 128
+                       *       keys, and at least describe().min_chunk (half the chunk of a
+                       *       max_kv_len request), so a much shorter request fills fewer chunks
+                       *       and its other chunks are empty;
                        * 0: the plan picks the number of chunks (describe().grid_y) and the
                        *    row-group size for this GPU from max_batch and max_kv_len; runs then
                        *    pass nsplit = 0 as well */
@@ -126,6 +129,7 @@ typedef struct {
   size_t workspace_bytes;
   int32_t resident_tile; /* 1: tensor-core kernel keeps each key tile resident (one gather per key and
                           * row group); 0: value blocks gathered twice, or the CUDA-core kernel */
+  int32_t min_chunk;     /* shortest chunk of any request, in keys (see nsplit) */
 } mla_verify_plan_info;
 
 /*

@@ -43,7 +43,8 @@ class MlaVerifyPlanInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32), ("keys_per_tile", ctypes.c_int32),
                 ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),
                 ("merge_blocks", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_size_t), ("resident_tile", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_size_t), ("resident_tile", ctypes.c_int32),
+                ("min_chunk", ctypes.c_int32)]
 
 
 class MlaVerifyError(RuntimeError):

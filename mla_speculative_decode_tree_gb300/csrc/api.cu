@@ -24,6 +24,7 @@ struct mla_verify_plan_s {
   int64_t rows_max;
   bool fused;  // the split kernel merges (MLA_VERIFY_FUSED_MERGE on the tensor-core kernel)
   int splits;  // KV chunks per request = grid dimension = partials per row (nsplit, or the plan's count)
+  int min_chunk;  // shortest chunk of any request (keys)
   size_t off_cnt, off_lse, off_o, ws_bytes;  // [0, off_lse) must be zero between calls
   int merge_blocks;
   int smem;
@@ -73,7 +74,7 @@ double tile_us(bool resident, int nq) { return resident ? 5.1 : nq >= 96 ? 5.9 :
 double est_us(int64_t rows_b, int64_t max_kv_len, int max_batch, int nsplit, int nq, bool resident, double sms) {
   constexpr double kCtaUs = 5.0, kMergeUs = 2.0, kMergeBytesPerUs = 3.0e6;
   const double groups = (double)((rows_b + nq - 1) / nq);
-  const int64_t chunk = chunk_len(max_kv_len, nsplit);
+  const int64_t chunk = chunk_len(max_kv_len, nsplit, kMinChunk);
   const double per = (double)(chunk / kKeysPerTile);                 // tiles in a chunk of the longest request
   const double splits = (double)((max_kv_len + chunk - 1) / chunk);  // its non-empty chunks
   const double tiles_max = (double)((max_kv_len + kKeysPerTile - 1) / kKeysPerTile);
@@ -316,6 +317,15 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
     const int64_t want = std::max<int64_t>(1, (int64_t)device_sm_count() * 4 / std::max<int64_t>(rows, 1));
     pl->splits = p.nsplit > 0 ? p.nsplit : (int)std::min<int64_t>(want, tiles);
   }
+  // Chunks are never shorter than half the longest request's chunk: a
+  // request much shorter than max_kv_len then takes fewer, longer chunks and
+  // writes fewer partials, while the longest request -- the launch's
+  // critical path -- keeps its chunks.
+  {
+    const int64_t longest = chunk_len(p.max_kv_len, pl->splits, kMinChunk);
+    const int64_t half = longest / 2 / kKeysPerTile * kKeysPerTile;
+    pl->min_chunk = (int)(half < kMinChunk ? kMinChunk : half);
+  }
   pl->groups = (int)((rows_b + pl->nq - 1) / pl->nq);
   pl->smem = pl->kernel ? tc_smem(pl->nq, pl->resident) : 0;
 
@@ -342,6 +352,7 @@ int mla_verify_plan_describe(mla_verify_plan_t pl, mla_verify_plan_info* info) {
   info->grid_z = pl->p.max_batch;
   info->merge_blocks = pl->merge_blocks;
   info->smem_bytes = pl->smem;
+  info->min_chunk = pl->min_chunk;
   info->workspace_bytes = pl->ws_bytes;
   return MLA_VERIFY_OK;
 }
@@ -378,6 +389,7 @@ int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_
   a.H = pl->p.num_heads;
   a.T = pl->p.q_len;
   a.nsplit = pl->splits;
+  a.min_chunk = pl->min_chunk;
   a.pool_rows = pl->p.pool_rows;
   a.rows_max = pl->rows_max;
   a.scale_log2 = sm_scale * 1.4426950408889634f;

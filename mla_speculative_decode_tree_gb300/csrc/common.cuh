@@ -33,6 +33,7 @@ struct SplitArgs {
   const int32_t* qo_indptr;      // [B+1] first token row of each request, or null: request b owns
                                  // token rows b*T .. b*T+T-1 (T = the plan's q_len, the maximum)
   int32_t batch, H, T, nsplit;
+  int32_t min_chunk;             // shortest chunk (keys, a multiple of the tile) for any request
   int32_t test_stall;            // test only: the gather never signals block 0 (waits time out)
   int64_t pool_rows;
   int64_t rows_max;              // max_batch*T*H: row stride of one split's partials
@@ -67,11 +68,13 @@ struct MergeArgs {
   uint32_t* status;  // header words 0 (accumulated) and 1 (last call)
 };
 
-// Key range of split s for a request with L keys: [s*chunk, min(L,(s+1)*chunk)).
-__host__ __device__ inline int64_t chunk_len(int64_t L, int nsplit) {
+// Key range of split s for a request with L keys: [s*chunk, min(L,(s+1)*chunk)),
+// with chunk = ceil(L/nsplit) rounded up to the tile and at least min_chunk
+// (a multiple of the tile fixed by the plan, at least kMinChunk).
+__host__ __device__ inline int64_t chunk_len(int64_t L, int nsplit, int64_t min_chunk) {
   int64_t per = (L + nsplit - 1) / nsplit;
   int64_t c = (per + kKeysPerTile - 1) / kKeysPerTile * kKeysPerTile;
-  return c < kMinChunk ? kMinChunk : c;
+  return c < min_chunk ? min_chunk : c;
 }
 
 #if defined(__CUDACC__)

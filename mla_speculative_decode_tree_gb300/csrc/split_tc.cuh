@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(TcCfg<NQ, kMode>::kThreads, 1)
   const int64_t P = (int64_t)a.kv_indptr[b + 1] - kv_base;
   const RequestTokens rq = request_tokens(a, b);
   const int64_t L = P + rq.n;
-  const int64_t chunk = chunk_len(L, a.nsplit);
+  const int64_t chunk = chunk_len(L, a.nsplit, a.min_chunk);
   const int64_t j0 = (int64_t)s_idx * chunk;
   const int64_t j1 = (j0 + chunk < L) ? j0 + chunk : L;
   const int rows_b = rq.n * a.H;
@@ -737,6 +737,9 @@ __global__ void __launch_bounds__(TcCfg<NQ, kMode>::kThreads, 1)
     }
 
     // ---- epilogue: l, LSE, O = O^T / l ----------------------------------------
+    // The sums need no MMA: reduce them while the last PV runs.
+    if (tid < 2 * NQ) ctl.red[tid & 1][tid >> 1] = l_half;
+    warp_columns_to_smem<HC, false>(acc_r, &ctl.red2[quad][c0], lane);
     if (!my_abort) {
       if constexpr (kLandOnce)
         my_abort = !mbar_wait(&ctl.pv_last, 0, &ctl.abort, a.status);
@@ -746,8 +749,6 @@ __global__ void __launch_bounds__(TcCfg<NQ, kMode>::kThreads, 1)
     tc::fence_after_sync();
     const bool wa = __any_sync(0xffffffffu, my_abort) || ctl.abort;
     if (lane == 0) ctl.flag[nt & 1][warp] = wa ? 2 : 0;
-    if (tid < 2 * NQ) ctl.red[tid & 1][tid >> 1] = l_half;
-    warp_columns_to_smem<HC, false>(acc_r, &ctl.red2[quad][c0], lane);
     named_bar_sync(1, kSoftmaxThreads);
     int f = 0;
 #pragma unroll
