@@ -131,6 +131,20 @@ def traffic_key(workload: str, nsplit=None) -> str:
     return workload if nsplit is None else "%s@nsplit%d" % (workload, nsplit)
 
 
+def ncu_record(workload: str):
+    """The committed ncu record of a workload's split kernel, if it matches this source."""
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent
+
+
 def ncu_traffic(workload: str):
     """DRAM bytes per split-kernel launch from the committed ncu summary, if it matches this source."""
     path = os.path.join(ROOT, "profiles", "split_kernel_traffic.json")
@@ -455,6 +469,29 @@ def summarize(res, peaks):
         status=res["status"], tree_mask=res.get("tree_mask"))
 
 
+def run_profile_target(args):
+    """A clean target for ncu: NAME's verify call (the varlen entry point when
+    the workload has per-request token counts), warmup + steps launches of the
+    split kernel in a row, each after an L2 flush, and nothing else on the
+    device; prints the plan."""
+    import torch
+    from __graft_entry__ import build
+    from mla_speculative_decode_tree_gb300 import binding as B
+    from mla_speculative_decode_tree_gb300 import workloads as W
+    build()
+    wl = W.make_workload(W.CONFIGS[args.ncu_workload])
+    d = B.device_inputs(wl)
+    v = B.verifier_for(wl, nsplit=args.nsplit)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup + args.steps):
+        flush.zero_()
+        v.run(d, wl["B"], wl["sm_scale"])
+    torch.cuda.synchronize()
+    info = v.plan.describe()
+    print(json.dumps({"workload": args.ncu_workload, "status": v.status(), "rows_per_cta": info.rows_per_cta,
+                      "resident_tile": info.resident_tile, "grid": [info.grid_x, info.grid_y, info.grid_z]}))
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -488,6 +525,9 @@ def run_gpu(args):
     from mla_speculative_decode_tree_gb300 import binding as B
     from mla_speculative_decode_tree_gb300 import workloads as W
     cfg = W.CONFIGS[args.workload]
+    if cfg.T_range is not None:
+        raise SystemExit("bench.py: %s has per-request token counts; it is timed in the sweep, not as the headline"
+                         % args.workload)
     wl = W.make_workload(cfg)
     d = B.device_inputs(wl)
     v = B.verifier_for(wl, nsplit=args.nsplit)
@@ -586,7 +626,10 @@ def run_gpu(args):
             try:
                 res = measure_workload(torch, name, min(args.steps, 30), 3, flush, stream)
                 s = summarize(res, peaks)
-                s["traffic"] = ncu_traffic(name)
+                rec = ncu_record(name) or {}
+                s["traffic"] = rec.get("dram_bytes_per_launch")
+                s["tensor_pipe_pct"] = rec.get("tensor_pipe_pct")
+                s["dram_throughput_pct"] = rec.get("dram_throughput_pct")
                 sweep[name] = {k: (round(x, 4) if isinstance(x, float) else x) for k, x in s.items()}
                 del res
             except Exception as exc:  # keep the headline line even if one sweep entry fails
@@ -711,10 +754,15 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+PCT_METRICS = {"sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed": "tensor_pipe_pct",
+               "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed": "dram_throughput_pct"}
+
+
 def record_traffic(csv_path: str, workload: str) -> dict:
     """Store the split kernel's DRAM bytes per launch from an ncu CSV capture
-    (metrics dram__bytes_read.sum and dram__bytes_write.sum) under the current
-    kernel source hash, for the `traffic` field of later runs."""
+    (metrics dram__bytes_read.sum and dram__bytes_write.sum, and when present
+    the tensor-pipe and DRAM-throughput percentages of PCT_METRICS) under the
+    current kernel source hash, for the `traffic` fields of later runs."""
     import csv
     scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
     per_launch = {}
@@ -724,11 +772,14 @@ def record_traffic(csv_path: str, workload: str) -> dict:
             if "split_tc_kernel" not in r.get("Kernel Name", "") and "split_simt_kernel" not in r.get("Kernel Name", ""):
                 continue
             name = r.get("Metric Name", "")
+            if name in PCT_METRICS:
+                per_launch.setdefault(r["ID"], {})[name] = float(r["Metric Value"].replace(",", ""))
+                continue
             if name not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
                 continue
             v = float(r["Metric Value"].replace(",", "")) * scale.get(r.get("Metric Unit", "byte"), 1)
             per_launch.setdefault(r["ID"], {})[name] = v
-    launches = [d for d in per_launch.values() if len(d) == 2]
+    launches = [d for d in per_launch.values() if "dram__bytes_read.sum" in d and "dram__bytes_write.sum" in d]
     if not launches:
         raise SystemExit("no split-kernel launch with both DRAM metrics in %s" % csv_path)
     bytes_avg = sum(d["dram__bytes_read.sum"] + d["dram__bytes_write.sum"] for d in launches) / len(launches)
@@ -742,6 +793,10 @@ def record_traffic(csv_path: str, workload: str) -> dict:
                      "launches": len(launches),
                      "read_bytes": int(round(sum(d["dram__bytes_read.sum"] for d in launches) / len(launches))),
                      "write_bytes": int(round(sum(d["dram__bytes_write.sum"] for d in launches) / len(launches)))}
+    for metric, key in PCT_METRICS.items():
+        vals = [d[metric] for d in launches if metric in d]
+        if vals:
+            rec[workload][key] = round(sum(vals) / len(vals), 2)
     os.makedirs(os.path.dirname(path), exist_ok=True)
     with open(path, "w") as f:
         json.dump(rec, f, indent=1, sort_keys=True)
@@ -761,6 +816,8 @@ def main(argv=None):
     ap.add_argument("--clock-log", metavar="CSV", default=None,
                     help="also write every nvidia-smi clock sample to this file")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ncu-workload", metavar="NAME", default=None,
+                    help="profiling target: run only NAME's verify call (its own entry point), warmup+steps times")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="store the split kernel's DRAM bytes per launch from an ncu CSV for --workload, then exit")
     ap.add_argument("--nsplit", type=int, default=None,
@@ -775,6 +832,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.ncu_workload:
+        run_profile_target(args)
     elif args.relocation_only:
         import torch
         from __graft_entry__ import build
