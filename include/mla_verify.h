@@ -105,8 +105,8 @@ typedef struct {
   int32_t max_kv_len; /* >= max_b (P_b + T); documents the longest request (chunk size is per request) */
   int64_t pool_rows;  /* rows in kv_pool; keys resolving outside [0, pool_rows) are left out and flagged */
   int32_t nsplit;     /* >= 1: KV chunks per request = partials per output row (fixed grid
-                       *       dimension); request b's chunk is ceil(L_b/nsplit) rounded up to 128
-                       *       keys, and at least describe().min_chunk (half the chunk of a
+                       *       dimension); request b's chunk is ceil(L_b/nsplit) rounded up to
+                       *       describe().chunk_granule keys, and at least describe().min_chunk (half the chunk of a
                        *       max_kv_len request), so a much shorter request fills fewer chunks
                        *       and its other chunks are empty;
                        * 0: the plan picks the number of chunks (describe().grid_y) and the
@@ -122,7 +122,7 @@ typedef struct {
 typedef struct {
   int32_t kernel;        /* 1 = tcgen05 tensor-core split kernel, 0 = CUDA-core split kernel */
   int32_t rows_per_cta;  /* query rows (token x head pairs) one split CTA covers */
-  int32_t keys_per_tile; /* keys per pipeline tile (chunk sizes are multiples of it) */
+  int32_t keys_per_tile; /* keys per pipeline tile (128) */
   int32_t grid_x, grid_y, grid_z; /* split grid: row groups x KV chunks per request x max_batch */
   int32_t merge_blocks;  /* merge grid size; 0 when the split kernel merges (MLA_VERIFY_FUSED_MERGE) */
   int32_t smem_bytes;    /* dynamic shared memory of the split kernel */
@@ -130,6 +130,7 @@ typedef struct {
   int32_t resident_tile; /* 1: tensor-core kernel keeps each key tile resident (one gather per key and
                           * row group); 0: value blocks gathered twice, or the CUDA-core kernel */
   int32_t min_chunk;     /* shortest chunk of any request, in keys (see nsplit) */
+  int32_t chunk_granule; /* chunk lengths are multiples of it: 64 keys (resident tiles, one request) or 128 */
 } mla_verify_plan_info;
 
 /*

@@ -44,7 +44,7 @@ class MlaVerifyPlanInfo(ctypes.Structure):
                 ("grid_x", ctypes.c_int32), ("grid_y", ctypes.c_int32), ("grid_z", ctypes.c_int32),
                 ("merge_blocks", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_size_t), ("resident_tile", ctypes.c_int32),
-                ("min_chunk", ctypes.c_int32)]
+                ("min_chunk", ctypes.c_int32), ("chunk_granule", ctypes.c_int32)]
 
 
 class MlaVerifyError(RuntimeError):

@@ -12,7 +12,8 @@ constexpr int kDLatent = 512;
 constexpr int kDRope = 64;
 constexpr int kDRow = kDLatent + kDRope;  // 576 bf16 = 1152 bytes per pool row
 constexpr int kRowBytes = kDRow * 2;
-constexpr int kKeysPerTile = 128;         // keys per pipeline tile; chunk sizes are multiples of it
+constexpr int kKeysPerTile = 128;         // keys per pipeline tile
+constexpr int kHalfTile = 64;             // finest chunk granule: a chunk may end in a half tile
 constexpr int kMinChunk = 128;
 constexpr int kMaxQLen = 64;
 constexpr int kWsHeader = 256;            // bytes: [0] status accumulated by split, [1] status of the last merge
@@ -33,7 +34,8 @@ struct SplitArgs {
   const int32_t* qo_indptr;      // [B+1] first token row of each request, or null: request b owns
                                  // token rows b*T .. b*T+T-1 (T = the plan's q_len, the maximum)
   int32_t batch, H, T, nsplit;
-  int32_t min_chunk;             // shortest chunk (keys, a multiple of the tile) for any request
+  int32_t min_chunk;             // shortest chunk (keys, a multiple of chunk_granule) for any request
+  int32_t chunk_granule;         // chunk lengths are multiples of it: kKeysPerTile or kHalfTile
   int32_t test_stall;            // test only: the gather never signals block 0 (waits time out)
   int64_t pool_rows;
   int64_t rows_max;              // max_batch*T*H: row stride of one split's partials
@@ -69,11 +71,12 @@ struct MergeArgs {
 };
 
 // Key range of split s for a request with L keys: [s*chunk, min(L,(s+1)*chunk)),
-// with chunk = ceil(L/nsplit) rounded up to the tile and at least min_chunk
-// (a multiple of the tile fixed by the plan, at least kMinChunk).
-__host__ __device__ inline int64_t chunk_len(int64_t L, int nsplit, int64_t min_chunk) {
+// with chunk = ceil(L/nsplit) rounded up to the plan's granule and at least
+// min_chunk (a multiple of the granule fixed by the plan, at least kMinChunk).
+// The granule is a power of two.
+__host__ __device__ inline int64_t chunk_len(int64_t L, int nsplit, int64_t min_chunk, int granule = kKeysPerTile) {
   int64_t per = (L + nsplit - 1) / nsplit;
-  int64_t c = (per + kKeysPerTile - 1) / kKeysPerTile * kKeysPerTile;
+  int64_t c = (per + granule - 1) & ~(int64_t)(granule - 1);
   return c < min_chunk ? min_chunk : c;
 }
 

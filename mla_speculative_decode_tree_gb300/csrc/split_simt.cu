@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(32 * kSimtRowsPerCta) split_simt_kernel(SplitA
   const int64_t P = (int64_t)a.kv_indptr[b + 1] - kv_base;
   const RequestTokens rq = request_tokens(a, b);
   const int64_t L = P + rq.n;
-  const int64_t chunk = chunk_len(L, a.nsplit, a.min_chunk);
+  const int64_t chunk = chunk_len(L, a.nsplit, a.min_chunk, a.chunk_granule);
   const int64_t j0 = (int64_t)s * chunk;
   const int64_t j1 = (j0 + chunk < L) ? j0 + chunk : L;
   const int rows_b = rq.n * a.H;

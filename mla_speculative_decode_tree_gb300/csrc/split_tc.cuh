@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(TcCfg<NQ, kMode>::kThreads, 1)
   const int64_t P = (int64_t)a.kv_indptr[b + 1] - kv_base;
   const RequestTokens rq = request_tokens(a, b);
   const int64_t L = P + rq.n;
-  const int64_t chunk = chunk_len(L, a.nsplit, a.min_chunk);
+  const int64_t chunk = chunk_len(L, a.nsplit, a.min_chunk, a.chunk_granule);
   const int64_t j0 = (int64_t)s_idx * chunk;
   const int64_t j1 = (j0 + chunk < L) ? j0 + chunk : L;
   const int rows_b = rq.n * a.H;
@@ -316,8 +316,9 @@ __global__ void __launch_bounds__(TcCfg<NQ, kMode>::kThreads, 1)
     // Row ids: lane (jl, c8) resolves keys 4*(c8 + 8m) + jl, m = 0..3, which
     // are exactly the keys lanes 8*jl.. copy at iterations it = c8 + 8m; a
     // shuffle of own[it/8] from lane 8*jl + it%8 hands each copier its row.
-    // Keys past the split's end or resolving outside the pool are fetched from
-    // the split's first row (finite by contract); the softmax masks them.
+    // Keys resolving outside the pool are fetched from the split's first row
+    // (finite by contract); keys past the split's end (a closing half tile)
+    // are not fetched: their slots are zero-filled.  The softmax masks both.
     // The index loads run a tile ahead of their use (ids of tile t+1 are
     // loaded while tile t is fetched), so no gather warp waits on an index
     // load between tiles.
@@ -348,12 +349,14 @@ __global__ void __launch_bounds__(TcCfg<NQ, kMode>::kThreads, 1)
 #pragma unroll
       for (int m = 0; m < kM; ++m) {
         prev[m] = own[m];
-        int64_t rr = rsub;
+        int64_t rr = -1;  // past the split's end
         if (key_of(tile, m) < j1) {
-          if (raw_cur[m] >= 0 && raw_cur[m] < a.pool_rows)
+          if (raw_cur[m] >= 0 && raw_cur[m] < a.pool_rows) {
             rr = raw_cur[m];
-          else
+          } else {
+            rr = rsub;
             bad = 1;
+          }
         }
         own[m] = (int)rr;
         raw_cur[m] = raw_nxt[m];
@@ -369,7 +372,8 @@ __global__ void __launch_bounds__(TcCfg<NQ, kMode>::kThreads, 1)
       for (int it = 0; it < kKeys / 4; ++it) {
         const int row = __shfl_sync(0xffffffffu, r[it >> 3], 8 * jl + (it & 7));
         const int swz = (c8 ^ (4 * (it & 1) + jl)) << 4;  // key (4*it + jl) mod 8 = 4*(it%2) + jl
-        cp_async16(base + it * 512 + swz, src0 + (int64_t)row * kDRow, 16u);
+        // row < 0: zero-fill, nothing read (the address stays inside the pool)
+        cp_async16(base + it * 512 + swz, src0 + (int64_t)(row < 0 ? 0 : row) * kDRow, row < 0 ? 0u : 16u);
       }
       cp_async_arrive(&ctl.full[slot]);
     };

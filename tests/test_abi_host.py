@@ -183,6 +183,23 @@ def test_relocate_host_validation(lib):
     assert lib.mla_verify_relocate_kv(None, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 1 << 30, None) == B.MLA_VERIFY_EINVAL
 
 
+@pytest.mark.parametrize("B_,kv,ns,flags,granule,min_chunk", [
+    (1, 4105, 16, 0, 64, 128),         # one request, resident tiles: chunks of 320 keys (2.5 tiles)
+    (1, 185009, 64, 0, 64, 1472),      # chunk 2944 keys; the shortest is half of it, in 64-key steps
+    (1, 4105, 16, R, 128, 128),        # value refetch: whole tiles
+    (16, 32777, 16, 0, 128, 1024),     # several requests: whole tiles
+    (1, 4105, 16, B.MLA_VERIFY_FORCE_SIMT, 128, 128),
+])
+def test_chunk_granule(lib, B_, kv, ns, flags, granule, min_chunk):
+    """Chunk lengths are multiples of the plan's granule: half a tile only
+    for one request in resident mode."""
+    H = 8 if kv > 100000 else 64
+    info = plan(max_batch=B_, num_heads=H, q_len=9, max_kv_len=kv, pool_rows=1 << 20, nsplit=ns,
+                flags=flags).describe()
+    assert (info.chunk_granule, info.min_chunk) == (granule, min_chunk)
+    assert info.min_chunk % info.chunk_granule == 0
+
+
 def test_auto_split_plan(lib):
     """nsplit = 0: the plan picks the number of chunks per request (the grid's
     split dimension) and sizes the workspace by it."""

@@ -227,7 +227,7 @@ def test_split_merge_invariance(oracle_lib):
     """Split-then-merge (the pages' organisation) equals the direct form for any split count."""
     wl = W.tiny_workload(B=2, H=2, T=9, prefix_lens=[300, 41], pool_rows=512, seed=10)
     o, lse = oracle_lib.verify(wl)
-    for nsplit, granule, min_chunk in ((1, 1, 1), (2, 1, 1), (3, 128, 128), (7, 1, 1), (16, 128, 128),
+    for nsplit, granule, min_chunk in ((1, 1, 1), (2, 1, 1), (3, 128, 128), (3, 64, 128), (7, 1, 1), (16, 128, 128),
                                        (64, 1, 1)):
         o2, lse2 = oracle_lib.verify_split_merge(wl, nsplit, granule, min_chunk)
         np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)

@@ -85,6 +85,7 @@ ADHOC = [
     (4, 8, 9, [3000, 100, 5000, 64], 16384, 64, "random"),  # 72 rows, 256 CTAs -> 48 rows, or one 96-row group
     (2, 64, 9, [5000, 3000], 16384, 64, "random"),    # 576 rows -> 64-row groups, or 96
     (1, 2, 64, [500], 4096, 2, "random"),             # q_len 64 (the maximum): 24 tokens per group
+    (1, 16, 9, [1400], 4096, 8, "random"),            # one request: chunks of 192 keys end in a half tile
 ]
 
 
@@ -95,6 +96,12 @@ def test_parity_adhoc(case, flags):
     wl = W.tiny_workload(B=Bn, H=H, T=T, prefix_lens=prefixes, pool_rows=pool, seed=sum(prefixes) + H,
                          tree=tree, nsplit=nsplit)
     check_full(wl, flags, what=str(case))
+
+
+def test_a_half_tile_chunk_is_exercised():
+    """One ad-hoc case plans chunks that end in a half tile (64-key granule)."""
+    info = B.mla_verify_plan(1, 16, 9, 1409, 4096, 8, 0).describe()
+    assert info.chunk_granule == 64 and info.resident_tile == 1  # ceil(1409 / 8) = 177 -> 192 keys
 
 
 def test_every_mode_and_row_group_size_is_exercised():
