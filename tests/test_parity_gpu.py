@@ -180,6 +180,21 @@ def test_nsplit_invariance(nsplit, flags):
     compare(o, lse, o_ref, lse_ref, "nsplit=%d" % nsplit)
 
 
+@pytest.mark.parametrize("flags", MODES[:2], ids=MODE_IDS[:2])
+@pytest.mark.parametrize("nsplit", [1, 3, 7, 16, 40])
+def test_nsplit_invariance_one_request(nsplit, flags):
+    """One request (64 rows): in resident mode the chunks are multiples of 64 keys, so most
+    of these end in a half tile (3004 keys: 1024, 448, 192 and 128-key chunks)."""
+    from oracle import ref
+    wl = W.tiny_workload(B=1, H=16, T=4, prefix_lens=[3000], pool_rows=8192, seed=22, nsplit=nsplit)
+    info = B.mla_verify_plan(1, 16, 4, 3004, 8192, nsplit, flags).describe()
+    assert info.chunk_granule == (128 if flags else 64)
+    o, lse, st, _ = gpu_run(wl, flags=flags)
+    assert st == 0
+    o_ref, lse_ref = ref.verify(wl, nthreads=NTHREADS)
+    compare(o, lse, o_ref, lse_ref, "one request, nsplit=%d" % nsplit)
+
+
 def encoded_pool(pool_rows, rng):
     """Rows whose first three latent values spell their own index (exact in bf16)."""
     pool = np.zeros((pool_rows, 576), dtype=np.float32)
@@ -193,7 +208,8 @@ def encoded_pool(pool_rows, rng):
 
 
 @pytest.mark.parametrize("flags", MODES, ids=MODE_IDS)
-@pytest.mark.parametrize("H,T,prefixes", [(64, 9, [300, 1001, 7]), (8, 9, [129, 0, 640]), (3, 5, [40, 9, 300])])
+@pytest.mark.parametrize("H,T,prefixes", [(64, 9, [300, 1001, 7]), (8, 9, [129, 0, 640]), (3, 5, [40, 9, 300]),
+                                         (16, 4, [2900])])  # one request: 1472-key chunks end in a half tile
 def test_row_selection_and_mask_decoding_exact(H, T, prefixes, flags):
     """One visible key per draft token at a chosen position: O must be that row, bit for bit."""
     rng = np.random.default_rng(H * 100 + T)
@@ -207,6 +223,8 @@ def test_row_selection_and_mask_decoding_exact(H, T, prefixes, flags):
         js[0] = L - 1
         if P > 0:
             js[min(1, T - 1)] = P - 1
+        if T > 2 and L > 1472:
+            js[2] = 1471  # the last key of the first chunk when chunks are 1472 keys (one request, nsplit 2)
         m[np.arange(T), js] = True
         dense.append(m)
         for i in range(T):
