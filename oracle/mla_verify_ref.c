@@ -63,7 +63,11 @@ enum {
   MUT_NO_SCALE = 7,           /* sm_scale not applied                      */
   MUT_V_SHIFT = 8,            /* values taken from columns 64..575         */
   MUT_DRAFT_REVERSED = 9,     /* draft rows read in reverse order          */
-  MUT_SOFTMAX_SIGN = 10       /* exp(m - s) instead of exp(s - m)          */
+  MUT_SOFTMAX_SIGN = 10,      /* exp(m - s) instead of exp(s - m)          */
+  /* per-request draft counts (qo_indptr given) */
+  MUT_QO_DRAFT_UNIFORM = 11,  /* draft rows at out_cache_loc[b*T + t]      */
+  MUT_QO_QROW_UNIFORM = 12,   /* query row b*T + i instead of qo_indptr[b]+i */
+  MUT_QO_MASK_STRIDE_T = 13   /* mask row stride P_b + T (the maximum)     */
 };
 
 static double bf16_to_f64(uint16_t b) {
@@ -129,7 +133,8 @@ static int64_t key_row(const problem_t* p, int b, int64_t P, int64_t j) {
   } else {
     int64_t t = j - P;
     if (p->mutation == MUT_DRAFT_REVERSED) t = q_count(p, b) - 1 - t;
-    r = p->out_cache_loc[q_start(p, b) + t];
+    const int64_t base = (p->mutation == MUT_QO_DRAFT_UNIFORM) ? (int64_t)b * p->T : q_start(p, b);
+    r = p->out_cache_loc[base + t];
   }
   if (r < 0 || r >= p->pool_rows) return -1;
   return r;
@@ -137,7 +142,7 @@ static int64_t key_row(const problem_t* p, int b, int64_t P, int64_t j) {
 
 static int key_visible(const problem_t* p, int b, int i, int64_t P, int64_t j) {
   int64_t L = P + q_count(p, b);
-  int64_t stride = (p->mutation == MUT_MASK_STRIDE_PREFIX) ? P : L;
+  int64_t stride = (p->mutation == MUT_MASK_STRIDE_PREFIX) ? P : (p->mutation == MUT_QO_MASK_STRIDE_T) ? P + p->T : L;
   int bb = b;
   if (p->mutation == MUT_MASK_INDPTR_NEXT) bb = (b + 1 < p->B) ? b + 1 : b;
   int64_t bit = (int64_t)p->mask_indptr[bb] + (int64_t)i * stride + j;
@@ -171,7 +176,7 @@ static int attend_range(const problem_t* p, int b, int i, int h, int64_t j0, int
   int64_t P = p->kv_indptr[b + 1] - p->kv_indptr[b];
   int64_t L = (p->mutation == MUT_PREFIX_ONLY) ? P : P + q_count(p, b);
   if (j1 > L) j1 = L;
-  int64_t qrow = q_start(p, b) + i;
+  int64_t qrow = (p->mutation == MUT_QO_QROW_UNIFORM) ? (int64_t)b * p->T + i : q_start(p, b) + i;
   double m = -INFINITY;
   for (int64_t j = j0; j < j1; ++j) {
     s_buf[j - j0] = -INFINITY;

@@ -95,3 +95,57 @@ def test_varlen_split_merge_identity(oracle_lib, nsplit):
     o2, l2 = oracle_lib.verify_split_merge(wl, nsplit=nsplit, granule=4, min_chunk=4, nthreads=2)
     np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
     np.testing.assert_allclose(l2, lse, rtol=0, atol=1e-12)
+
+
+# ---- planted mistakes in the per-request indexing -------------------------
+# Each plants one plausible error of the varlen indexing in the C oracle
+# (mutation codes of oracle/mla_verify_ref.c) and must fail one of the pins
+# above, evaluated on the same workloads.
+
+VARLEN_MUTATIONS = {11: "draft rows at b*T", 12: "query row b*T + i", 13: "mask row stride P_b + T_max"}
+
+
+def _padded(wl):
+    """The workload with its packed mask padded, so a wrong (larger) mask
+    stride still reads inside the buffer."""
+    pad = np.zeros(wl["B"] * wl["T"] * wl["T"] // 8 + 16, np.uint8)
+    return dict(wl, custom_mask=np.concatenate([wl["custom_mask"], pad]))
+
+
+def _pin_requests_alone(oracle_lib, mutation):
+    wl = _padded(_varlen(1))
+    o, lse = oracle_lib.verify(wl, nthreads=2, mutation=mutation)
+    qo = wl["qo_indptr"]
+    for b in range(wl["B"]):
+        if int(qo[b + 1] - qo[b]) == 0:
+            continue
+        one = _request_alone(wl, b)
+        o1, l1 = oracle_lib.verify(one, nthreads=2)
+        rows = slice(int(qo[b]) * H, int(qo[b + 1]) * H)
+        if not (np.array_equal(o[rows], o1) and np.array_equal(lse[rows], l1)):
+            return False
+    return True
+
+
+def _pin_brute(oracle_lib, mutation):
+    wl = _padded(_varlen(3, T_list=(2, 5, 0, 4), prefix=(9, 0, 13, 6), pool_rows=256))
+    o, lse = oracle_lib.verify(wl, nthreads=2, mutation=mutation)
+    ob, lb = brute.brute_verify(wl)
+    return bool(np.allclose(o, np.array(ob), rtol=0, atol=1e-12) and np.allclose(lse, np.array(lb), rtol=0, atol=1e-12))
+
+
+def test_varlen_pins_hold_for_the_oracle(oracle_lib):
+    assert _pin_requests_alone(oracle_lib, 0) and _pin_brute(oracle_lib, 0)
+
+
+@pytest.mark.parametrize("mutation", sorted(VARLEN_MUTATIONS), ids=[VARLEN_MUTATIONS[k] for k in sorted(VARLEN_MUTATIONS)])
+def test_varlen_planted_mistakes_fail_a_pin(oracle_lib, mutation):
+    failed = []
+    for pin in (_pin_requests_alone, _pin_brute):
+        try:
+            ok = pin(oracle_lib, mutation)
+        except (AssertionError, ValueError):
+            ok = False
+        if not ok:
+            failed.append(pin.__name__)
+    assert failed, "mistake %r passed every varlen pin" % VARLEN_MUTATIONS[mutation]
