@@ -28,6 +28,7 @@ struct mla_verify_plan_s {
   int chunk_granule;  // chunk lengths are multiples of it (keys)
   size_t off_cnt, off_lse, off_o, ws_bytes;  // [0, off_lse) must be zero between calls
   int merge_blocks;
+  bool merge_quarter;  // merge with four warps per row (at most one wave of rows)
   int smem;
 };
 
@@ -343,7 +344,8 @@ int mla_verify_plan(const mla_verify_params* params, size_t* workspace_bytes, ml
                           : kWsHeader;
   pl->off_o = round_up(pl->off_lse + sizeof(float) * (size_t)pl->splits * (size_t)rows_max, 256);
   pl->ws_bytes = pl->off_o + sizeof(float) * (size_t)pl->splits * (size_t)rows_max * kDLatent;
-  pl->merge_blocks = pl->fused ? 0 : merge_blocks((int)rows_max);
+  pl->merge_quarter = merge_quarter_fits(rows_max, device_sm_count());
+  pl->merge_blocks = pl->fused ? 0 : merge_blocks((int)rows_max, pl->merge_quarter);
   *workspace_bytes = pl->ws_bytes;
   *out = pl;
   return MLA_VERIFY_OK;
@@ -451,6 +453,13 @@ int merge_impl(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, const int32_
   m.o = static_cast<__nv_bfloat16*>(o);
   m.lse = lse;
   m.status = reinterpret_cast<uint32_t*>(ws);
+  // Few rows: four warps per row.  When the partials also total at most
+  // ~48 MB (still in L2 after the split kernel), the merge loads them before
+  // their LSEs (an empty split's partial is read and dropped), one round trip
+  // fewer.
+  m.quarter = pl->merge_quarter ? 1 : 0;
+  m.speculative =
+      m.quarter && (uint64_t)pl->splits * (uint64_t)pl->rows_max * kDLatent * sizeof(float) <= (48ull << 20) ? 1 : 0;
   cudaError_t e = launch_merge(m, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_VERIFY_OK : cuda_fail(e);
 }

@@ -68,6 +68,8 @@ struct MergeArgs {
   __nv_bfloat16* o;  // [rows, 512]
   float* lse;        // [rows]
   uint32_t* status;  // header words 0 (accumulated) and 1 (last call)
+  int32_t quarter;      // four warps per row (few rows) instead of two
+  int32_t speculative;  // quarter layout: load the first 16 splits' partials before their LSEs
 };
 
 // Key range of split s for a request with L keys: [s*chunk, min(L,(s+1)*chunk)),
@@ -246,7 +248,8 @@ cudaError_t launch_tree_mask(const int32_t* parents, const int32_t* kv_indptr, c
                              cudaStream_t stream);
 cudaError_t launch_relocate(void* pool, const int32_t* kv_indptr, int32_t* kv_indices, const int32_t* dst_start,
                             int batch, int64_t pool_rows, int64_t max_keys, uint32_t* status, cudaStream_t stream);
-int merge_blocks(int rows);
+int merge_blocks(int rows, bool quarter);
+bool merge_quarter_fits(int64_t rows, int sms);
 
 constexpr int kSimtRowsPerCta = 8;  // one warp per query row
 

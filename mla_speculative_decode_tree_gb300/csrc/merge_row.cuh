@@ -105,4 +105,83 @@ __device__ __forceinline__ void merge_row_half(const float* part_lse, const floa
   if (half == 0 && lane == 0) lse_out[row] = M + logf(W);
 }
 
+// The same merge with one warp per quarter (128 latent columns) of the row,
+// lane l owning 4 columns, and the same arithmetic in the same order, so the
+// bits equal merge_row_half's.  Splits are taken 16 at a time; with kSpec the
+// first 16 splits' partials are loaded before their LSEs are known (one L2
+// round trip fewer), and a split with weight 0 -- an empty chunk whose partial
+// was never written -- has its loaded values replaced by 0 before use.  The
+// loads stay inside the workspace's nsplit partials.
+template <bool kSpec>
+__device__ __forceinline__ void merge_row_quarter(const float* part_lse, const float* part_o, int64_t rows_max,
+                                                  int nsplit, int64_t row, int quarter, int lane,
+                                                  __nv_bfloat16* o_out, float* lse_out) {
+  constexpr int G = 16;  // splits loaded ahead with kSpec
+  constexpr int U = 8;   // splits in flight per step otherwise; both divide 32
+  const int col = quarter * (kDLatent / 4) + 4 * lane;
+  const int64_t split_stride = rows_max * kDLatent;
+  const float* base = part_o + row * kDLatent + col;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 pre[kSpec ? G : 1];
+  if constexpr (kSpec) {
+#pragma unroll
+    for (int u = 0; u < G; ++u)
+      pre[u] = u < nsplit ? *reinterpret_cast<const float4*>(base + (int64_t)u * split_stride) : zero;
+  }
+  float M = -INFINITY;
+  for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, part_lse[(int64_t)s * rows_max + row]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  uint2* o = reinterpret_cast<uint2*>(o_out + row * kDLatent + col);
+  if (M == -INFINITY) {
+    *o = make_uint2(0, 0);
+    if (quarter == 0 && lane == 0) lse_out[row] = -INFINITY;
+    return;
+  }
+
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  auto fma4 = [&](float w, const float4& x) {
+    acc[0] = fmaf(w, x.x, acc[0]);
+    acc[1] = fmaf(w, x.y, acc[1]);
+    acc[2] = fmaf(w, x.z, acc[2]);
+    acc[3] = fmaf(w, x.w, acc[3]);
+  };
+  float W = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += 32) {
+    const int s = s0 + lane;
+    const float ls = s < nsplit ? part_lse[(int64_t)s * rows_max + row] : -INFINITY;
+    const float wl = ls == -INFINITY ? 0.f : expf(ls - M);
+    W += wl;
+    const int n = (nsplit - s0 < 32) ? nsplit - s0 : 32;
+    int k0 = 0;
+    if (kSpec && s0 == 0) {
+#pragma unroll
+      for (int u = 0; u < G; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wl, u);  // 0 past the last split
+        fma4(w, w != 0.f ? pre[u < G ? u : 0] : zero);
+      }
+      k0 = G;
+    }
+    for (; k0 < n; k0 += U) {
+      float wk[U];
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        wk[u] = __shfl_sync(0xffffffffu, wl, k0 + u);  // 0 past the last split
+        v[u] = wk[u] != 0.f ? *reinterpret_cast<const float4*>(base + (int64_t)(s0 + k0 + u) * split_stride) : zero;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) fma4(wk[u], v[u]);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+  const float inv = 1.f / W;
+  const __nv_bfloat162 h01 = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+  const __nv_bfloat162 h23 = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+  *o = make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+  if (quarter == 0 && lane == 0) lse_out[row] = M + logf(W);
+}
+
 }  // namespace mlav
