@@ -43,7 +43,22 @@ CASES = [
     (2, 16, 4, [5000, 129], 4),
     (4, 32, 3, [64, 1, 900, 4000], 32),
     (1, 8, 9, [20000], 64),              # few rows: 48-row groups
+    (1, 64, 9, [6000], 48),              # 576 rows, 48 splits: partials past 48 MB, loaded after their LSEs
 ]
+
+
+def test_every_merge_layout_is_compared():
+    """The cases cover the merge kernel's three forms: two warps per row (many
+    rows), four warps per row with the partials loaded ahead (partials <= 48 MB)
+    and four warps per row without (describe().merge_blocks: rows/4 or rows/2)."""
+    forms = set()
+    for Bn, H, T, P, nsplit in CASES:
+        info = B.mla_verify_plan(Bn, H, T, max(P) + T, 32768, nsplit, 0).describe()
+        rows = Bn * H * T
+        quarter = info.merge_blocks == (rows + 1) // 2
+        assert quarter or info.merge_blocks == (rows + 3) // 4
+        forms.add((quarter, quarter and nsplit * rows * 2048 <= 48 << 20))
+    assert forms == {(False, False), (True, True), (True, False)}, forms
 
 
 @pytest.mark.parametrize("mode", [0, B.MLA_VERIFY_REFETCH_VALUES], ids=["resident", "refetch"])
