@@ -385,7 +385,7 @@ int split_impl(mla_verify_plan_t pl, const void* q_nope_absorbed, const void* q_
     return rc;
   if ((rc = check_device()) != MLA_VERIFY_OK) return rc;
 
-  SplitArgs a;
+  SplitArgs a = {};
   a.q_nope = static_cast<const __nv_bfloat16*>(q_nope_absorbed);
   a.q_rope = static_cast<const __nv_bfloat16*>(q_rope);
   a.kv_pool = static_cast<const __nv_bfloat16*>(kv_pool);
@@ -441,7 +441,7 @@ int merge_impl(mla_verify_plan_t pl, int32_t batch, int32_t nsplit, const int32_
   if (!o || !lse || !aligned(o, 16) || !aligned(lse, 4)) return MLA_VERIFY_EINVAL;
   if ((rc = check_device()) != MLA_VERIFY_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  MergeArgs m;
+  MergeArgs m = {};
   m.rows = batch * pl->p.q_len * pl->p.num_heads;
   m.qo_indptr = qo_indptr;
   m.batch = batch;
