@@ -15,14 +15,14 @@
 // to 32, S^T at [4*S_o, 4*S_o + NQ).
 //
 // Shared memory holds Q (9 blocks of NQ rows x 64 columns, 128-byte
-// swizzled, K-major), P^T (NQ rows x 128 keys, K-major; tile t writes it once
-// the MMA of tile t-1 has read it) and a ring of 16 KB
-// slots, each 128 keys x 64 columns of the gathered pool rows in the
-// 128-byte-swizzle atom (8 keys x 128 bytes).  That atom is at once the
-// K-major layout of the key operand and the MN-major layout of the value
-// operand, so the value blocks need no transposition.  The value blocks of a
-// tile are fetched a second time (after the next tile's key blocks) rather
-// than kept resident: a whole 128-key tile (144 KB) does not fit next to Q.
+// swizzled, K-major), P^T (NQ rows x 128 keys, K-major) and 16 KB slots, each
+// 128 keys x 64 columns of the gathered pool rows in the 128-byte-swizzle
+// atom (8 keys x 128 bytes).  That atom is at once the K-major layout of the
+// key operand and the MN-major layout of the value operand, so the value
+// blocks need no transposition.  A whole 128-key tile (144 KB) fits next to
+// Q only for NQ <= 64 (resident mode below); otherwise the slots form a ring
+// and a tile's value blocks are fetched a second time, after the next tile's
+// key blocks (value-refetch mode).
 //
 // Warp roles (512 threads; CG = 3 column groups for NQ = 96, else 2):
 //   warps 0..4CG-1  softmax.  Warp w reads TMEM lane quadrant w%4 (keys
